@@ -1,0 +1,827 @@
+// C ABI of the library (include/sv.h): resident weights, cached workspaces,
+// the forward-pass orchestration and the per-op entry points. Host code only;
+// every step of the forward pass runs in this library's kernels.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "../../synth/synth.h"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+thread_local std::string g_err;
+
+struct Runtime {
+  bool ready = false;
+  int device = -1;
+  int sms = 0;
+  int* dev_err = nullptr;
+};
+Runtime g_rt;
+long long g_launches = 0;
+
+// ------------------------------------------------------------ profiling
+struct ProfRec {
+  int kind;
+  double flops, bytes;
+  cudaEvent_t e0, e1;
+};
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_ev_pool;
+
+cudaEvent_t get_event() {
+  if (!g_ev_pool.empty()) {
+    cudaEvent_t e = g_ev_pool.back();
+    g_ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Counts one launch and, when profiling is on, brackets it with events.
+struct Launch {
+  bool on;
+  cudaStream_t stream = nullptr;
+  Launch(int kind, double flops, double bytes, cudaStream_t s) : on(g_prof_on) {
+    ++g_launches;
+    if (on) {
+      ProfRec r{kind, flops, bytes, get_event(), get_event()};
+      cudaEventRecord(r.e0, s);
+      g_prof.push_back(r);
+      stream = s;
+    }
+  }
+  ~Launch() {
+    if (on) cudaEventRecord(g_prof.back().e1, stream);
+  }
+};
+
+// ------------------------------------------------------------ model state
+struct Dims {
+  int T = 0, P = 0, D = 0, H = 0, F = 0, L = 0, Kp = 0;
+};
+
+struct LayerW {
+  __half *ln1_g, *ln1_b, *qkv_w, *qkv_b, *out_w, *out_b, *ln2_g, *ln2_b, *fc1_w, *fc1_b, *fc2_w, *fc2_b;
+  uint8_t *qkv_w8, *out_w8, *fc1_w8, *fc2_w8;
+};
+
+struct Weights {
+  bool ready = false;
+  Dims d;
+  void* arena = nullptr;
+  __half *patch_w = nullptr, *patch_b = nullptr, *pos = nullptr;
+  uint8_t* patch_w8 = nullptr;
+  std::vector<LayerW> layers;
+  __half *enc_ln_g = nullptr, *enc_ln_b = nullptr, *probe = nullptr, *mq_w = nullptr, *mq_b = nullptr,
+         *mkv_w = nullptr, *mkv_b = nullptr, *mo_w = nullptr, *mo_b = nullptr, *mln_g = nullptr, *mln_b = nullptr,
+         *mfc1_w = nullptr, *mfc1_b = nullptr, *mfc2_w = nullptr, *mfc2_b = nullptr;
+  uint8_t *probe8 = nullptr, *mq_w8 = nullptr, *mkv_w8 = nullptr, *mo_w8 = nullptr, *mfc1_w8 = nullptr,
+          *mfc2_w8 = nullptr;
+};
+Weights g_w;
+
+// Buffers and operand maps of the MAP head for one batch size and dtype.
+struct MapPlan {
+  GemmOperands q, kv, out, fc1, fc2;
+  __half* qv = nullptr;  // [D] projected probe
+  __half* KV = nullptr;  // [B*T, 2D]
+  void* a = nullptr;     // [B, D] pooled attention (f16 / e4m3)
+  __half* A = nullptr;   // [B, D]
+  void* Ya = nullptr;    // [B, D] LN(A)
+  void* Ha = nullptr;    // [B, F]
+};
+
+// Workspace and operand maps of the whole forward pass for one batch size and dtype.
+struct Plan {
+  int B = 0, fp8 = 0;
+  void* mem = nullptr;
+  size_t bytes = 0;
+  void* A0 = nullptr;     // [M, Kp] staged pixels
+  __half* X = nullptr;    // [M, D] residual stream
+  void* Y = nullptr;      // [M, D] LayerNorm output (GEMM operand)
+  __half* QKV = nullptr;  // [M, 3D]
+  void* O = nullptr;      // [M, D] attention output (GEMM operand)
+  void* Hh = nullptr;     // [M, F] GELU output (GEMM operand)
+  GemmOperands patch;
+  std::vector<GemmOperands> qkv, out, fc1, fc2;
+  CUtensorMap attn;
+  MapPlan map;
+};
+std::map<std::pair<int, int>, std::unique_ptr<Plan>> g_plans;      // sv_encode
+std::map<std::pair<int, int>, std::unique_ptr<Plan>> g_map_plans;  // sv_map_pool
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+void free_plans() {
+  for (auto& kv : g_plans) cudaFree(kv.second->mem);
+  for (auto& kv : g_map_plans) cudaFree(kv.second->mem);
+  g_plans.clear();
+  g_map_plans.clear();
+}
+
+void free_weights() {
+  free_plans();
+  if (g_w.arena) cudaFree(g_w.arena);
+  g_w = Weights();
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+#define SV_CHECK_CUDA(call, what)                      \
+  do {                                                 \
+    cudaError_t e_ = (call);                           \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+#define SV_TRY(call)            \
+  do {                          \
+    sv_status s_ = (call);      \
+    if (s_ != SV_OK) return s_; \
+  } while (0)
+
+// ------------------------------------------------------------ weights upload
+sv_status init_weights(uint64_t seed, const Dims& d) {
+  free_weights();
+  SV_TRY(ensure_runtime());
+  synth_dims sd;
+  sd.tokens = d.T;
+  sd.patch_dim = d.P;
+  sd.width = d.D;
+  sd.heads = d.H;
+  sd.mlp = d.F;
+  sd.layers = d.L;
+  const int n = synth_tensor_count(&sd);
+
+  // Every dense weight is stored [N, Kpad] K-major in F16, plus an E4M3 copy.
+  struct Slot {
+    synth_tensor info;
+    bool matrix;
+    int kpad;
+    size_t off16, off8;
+  };
+  std::vector<Slot> slots(static_cast<size_t>(n));
+  size_t total = 0, max_elems = 0;
+  for (int id = 0; id < n; ++id) {
+    Slot& s = slots[size_t(id)];
+    synth_tensor_info(&sd, id, &s.info);
+    const std::string name = s.info.name;
+    s.matrix = name.size() > 2 && name.compare(name.size() - 2, 2, "_w") == 0;
+    s.kpad = s.matrix ? (name == "patch_w" ? d.Kp : s.info.rows) : s.info.rows;
+    const size_t elems = size_t(s.info.cols) * size_t(s.kpad);
+    max_elems = elems > max_elems ? elems : max_elems;
+    s.off16 = total;
+    total = align_up(total + 2 * elems, 256);
+    s.off8 = 0;
+    if (s.matrix || name == "probe") {
+      s.off8 = total;
+      total = align_up(total + elems, 256);
+    }
+  }
+  void* arena = nullptr;
+  cudaError_t e = cudaMalloc(&arena, total);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_error("cudaMalloc of %zu bytes for weights failed: %s", total, cudaGetErrorString(e));
+    return SV_ERR_OOM;
+  }
+  g_w.arena = arena;
+  g_w.d = d;
+  g_w.layers.assign(size_t(d.L), LayerW{});
+  std::vector<uint16_t> host(max_elems);
+  char* base = static_cast<char*>(arena);
+  for (int id = 0; id < n; ++id) {
+    Slot& s = slots[size_t(id)];
+    const std::string name = s.info.name;
+    const size_t elems = size_t(s.info.cols) * size_t(s.kpad);
+    const int rc = s.matrix ? synth_fill_tensor_f16_t(seed, &sd, id, host.data(), s.kpad)
+                            : synth_fill_tensor_f16(seed, &sd, id, host.data());
+    if (rc != 0) {
+      set_error("synthetic generator failed for tensor %s", name.c_str());
+      return SV_ERR_INVALID_ARG;
+    }
+    __half* p16 = reinterpret_cast<__half*>(base + s.off16);
+    SV_CHECK_CUDA(cudaMemcpy(p16, host.data(), 2 * elems, cudaMemcpyHostToDevice), "weight upload");
+    uint8_t* p8 = s.off8 ? reinterpret_cast<uint8_t*>(base + s.off8) : nullptr;
+    if (p8) SV_TRY(quantize_launch(p16, p8, elems, nullptr));
+    const int l = s.info.layer;
+    if (l >= 0) {
+      LayerW& w = g_w.layers[size_t(l)];
+      if (name == "ln1_g") w.ln1_g = p16;
+      else if (name == "ln1_b") w.ln1_b = p16;
+      else if (name == "qkv_w") w.qkv_w = p16, w.qkv_w8 = p8;
+      else if (name == "qkv_b") w.qkv_b = p16;
+      else if (name == "out_w") w.out_w = p16, w.out_w8 = p8;
+      else if (name == "out_b") w.out_b = p16;
+      else if (name == "ln2_g") w.ln2_g = p16;
+      else if (name == "ln2_b") w.ln2_b = p16;
+      else if (name == "fc1_w") w.fc1_w = p16, w.fc1_w8 = p8;
+      else if (name == "fc1_b") w.fc1_b = p16;
+      else if (name == "fc2_w") w.fc2_w = p16, w.fc2_w8 = p8;
+      else if (name == "fc2_b") w.fc2_b = p16;
+    } else {
+      if (name == "patch_w") g_w.patch_w = p16, g_w.patch_w8 = p8;
+      else if (name == "patch_b") g_w.patch_b = p16;
+      else if (name == "pos") g_w.pos = p16;
+      else if (name == "enc_ln_g") g_w.enc_ln_g = p16;
+      else if (name == "enc_ln_b") g_w.enc_ln_b = p16;
+      else if (name == "probe") g_w.probe = p16, g_w.probe8 = p8;
+      else if (name == "map_q_w") g_w.mq_w = p16, g_w.mq_w8 = p8;
+      else if (name == "map_q_b") g_w.mq_b = p16;
+      else if (name == "map_kv_w") g_w.mkv_w = p16, g_w.mkv_w8 = p8;
+      else if (name == "map_kv_b") g_w.mkv_b = p16;
+      else if (name == "map_out_w") g_w.mo_w = p16, g_w.mo_w8 = p8;
+      else if (name == "map_out_b") g_w.mo_b = p16;
+      else if (name == "map_ln_g") g_w.mln_g = p16;
+      else if (name == "map_ln_b") g_w.mln_b = p16;
+      else if (name == "map_fc1_w") g_w.mfc1_w = p16, g_w.mfc1_w8 = p8;
+      else if (name == "map_fc1_b") g_w.mfc1_b = p16;
+      else if (name == "map_fc2_w") g_w.mfc2_w = p16, g_w.mfc2_w8 = p8;
+      else if (name == "map_fc2_b") g_w.mfc2_b = p16;
+    }
+  }
+  SV_CHECK_CUDA(cudaDeviceSynchronize(), "weight initialisation");
+  g_w.ready = true;
+  return SV_OK;
+}
+
+// ------------------------------------------------------------ plans
+// Two passes over the same sequence of take() calls: the first (base null)
+// sizes the workspace, the second hands out pointers into it.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  void* take(size_t bytes) {
+    void* p = base ? base + off : nullptr;
+    off = align_up(off + bytes, 256);
+    return p;
+  }
+};
+
+// Buffers of the MAP head (carved from `c`); xf is the encoder-output operand.
+sv_status build_map(MapPlan& m, Carver& c, const void* xf, int B, int fp8, bool carve_kv, __half* kv_alias) {
+  const Dims& d = g_w.d;
+  const size_t eb = fp8 ? 1 : 2;
+  m.qv = static_cast<__half*>(c.take(size_t(d.D) * 2));
+  m.KV = carve_kv ? static_cast<__half*>(c.take(size_t(B) * d.T * 2 * d.D * 2)) : kv_alias;
+  m.a = c.take(size_t(B) * d.D * eb);
+  m.A = static_cast<__half*>(c.take(size_t(B) * d.D * 2));
+  m.Ya = c.take(size_t(B) * d.D * eb);
+  m.Ha = c.take(size_t(B) * d.F * eb);
+  if (!c.base) return SV_OK;
+  SV_TRY(gemm_prepare(&m.q, fp8 ? (const void*)g_w.probe8 : g_w.probe, fp8 ? (const void*)g_w.mq_w8 : g_w.mq_w, 1,
+                      d.D, d.D, fp8));
+  SV_TRY(gemm_prepare(&m.kv, xf, fp8 ? (const void*)g_w.mkv_w8 : g_w.mkv_w, B * d.T, 2 * d.D, d.D, fp8));
+  SV_TRY(gemm_prepare(&m.out, m.a, fp8 ? (const void*)g_w.mo_w8 : g_w.mo_w, B, d.D, d.D, fp8));
+  SV_TRY(gemm_prepare(&m.fc1, m.Ya, fp8 ? (const void*)g_w.mfc1_w8 : g_w.mfc1_w, B, d.F, d.D, fp8));
+  SV_TRY(gemm_prepare(&m.fc2, m.Ha, fp8 ? (const void*)g_w.mfc2_w8 : g_w.mfc2_w, B, d.D, d.F, fp8));
+  return SV_OK;
+}
+
+sv_status alloc_carved(Carver& c, void** mem, size_t* bytes) {
+  cudaError_t e = cudaMalloc(mem, c.off);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_error("cudaMalloc of %zu bytes for the workspace failed: %s", c.off, cudaGetErrorString(e));
+    return SV_ERR_OOM;
+  }
+  // Defined contents for every buffer (pads and unused tails read as zero).
+  SV_CHECK_CUDA(cudaMemset(*mem, 0, c.off), "workspace clear");
+  *bytes = c.off;
+  c.base = static_cast<char*>(*mem);
+  c.off = 0;
+  return SV_OK;
+}
+
+sv_status get_plan(int B, int fp8, Plan** out) {
+  const auto key = std::make_pair(B, fp8);
+  auto it = g_plans.find(key);
+  if (it != g_plans.end()) {
+    *out = it->second.get();
+    return SV_OK;
+  }
+  const Dims& d = g_w.d;
+  const size_t M = size_t(B) * d.T, eb = fp8 ? 1 : 2;
+  std::unique_ptr<Plan> p(new Plan());
+  p->B = B;
+  p->fp8 = fp8;
+  Carver c{nullptr};
+  for (int pass = 0; pass < 2; ++pass) {
+    p->A0 = c.take(M * d.Kp * eb);
+    p->X = static_cast<__half*>(c.take(M * d.D * 2));
+    p->Y = c.take(M * d.D * eb);
+    p->QKV = static_cast<__half*>(c.take(M * 3 * d.D * 2));
+    p->O = c.take(M * d.D * eb);
+    p->Hh = c.take(M * d.F * eb);
+    SV_TRY(build_map(p->map, c, p->Y, B, fp8, false, p->QKV));
+    if (pass == 0) {
+      sv_status st = alloc_carved(c, &p->mem, &p->bytes);
+      if (st != SV_OK) return st;
+    }
+  }
+  const int Mi = int(M);
+  sv_status st = SV_OK;
+  auto fail = [&](sv_status s) {
+    cudaFree(p->mem);
+    return s;
+  };
+  if ((st = gemm_prepare(&p->patch, p->A0, fp8 ? (const void*)g_w.patch_w8 : g_w.patch_w, Mi, d.D, d.Kp, fp8)))
+    return fail(st);
+  p->qkv.resize(size_t(d.L));
+  p->out.resize(size_t(d.L));
+  p->fc1.resize(size_t(d.L));
+  p->fc2.resize(size_t(d.L));
+  for (int l = 0; l < d.L; ++l) {
+    const LayerW& w = g_w.layers[size_t(l)];
+    if ((st = gemm_prepare(&p->qkv[size_t(l)], p->Y, fp8 ? (const void*)w.qkv_w8 : w.qkv_w, Mi, 3 * d.D, d.D, fp8)) ||
+        (st = gemm_prepare(&p->out[size_t(l)], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8)) ||
+        (st = gemm_prepare(&p->fc1[size_t(l)], p->Y, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8)) ||
+        (st = gemm_prepare(&p->fc2[size_t(l)], p->Hh, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, Mi, d.D, d.F, fp8)))
+      return fail(st);
+  }
+  if ((st = attention_map(&p->attn, p->QKV, B, d.T, d.H))) return fail(st);
+  *out = p.get();
+  g_plans[key] = std::move(p);
+  return SV_OK;
+}
+
+// ------------------------------------------------------------ launches with accounting
+double gemm_flops(const GemmOperands& g, int k_logical) { return 2.0 * g.M * double(g.N) * double(k_logical); }
+double gemm_bytes(const GemmOperands& g, const GemmEpi& e, int k_logical) {
+  const double eb = g.fp8 ? 1.0 : 2.0;
+  double b = (double(g.M) + double(g.N)) * k_logical * eb + double(g.M) * g.N * (e.out_e4m3 ? 1.0 : 2.0);
+  if (e.residual) b += double(g.M) * g.N * 2.0;
+  return b;
+}
+
+sv_status run_gemm(const GemmOperands& g, const GemmEpi& e, int k_logical, cudaStream_t s) {
+  Launch L(kKindGemm, gemm_flops(g, k_logical), gemm_bytes(g, e, k_logical), s);
+  return gemm_launch(g, e, s);
+}
+
+sv_status run_ln(const __half* x, const __half* gm, const __half* bt, void* y, int rows, int out_e4m3,
+                 cudaStream_t s) {
+  const int D = g_w.d.D;
+  Launch L(kKindLN, 8.0 * rows * D, double(rows) * D * (2.0 + (out_e4m3 ? 1.0 : 2.0)), s);
+  return layernorm_launch(x, gm, bt, y, rows, D, 1e-6f, out_e4m3, s);
+}
+
+sv_status run_map(MapPlan& m, int B, int fp8, __half* out, cudaStream_t s) {
+  const Dims& d = g_w.d;
+  const float sc = fp8 ? 1.0f / 256.0f : 1.0f;
+  GemmEpi e;
+  e.scale = sc;
+  e.bias = g_w.mq_b;
+  e.out = m.qv;
+  SV_TRY(run_gemm(m.q, e, d.D, s));
+  e.bias = g_w.mkv_b;
+  e.out = m.KV;
+  SV_TRY(run_gemm(m.kv, e, d.D, s));
+  {
+    Launch L(kKindMapAttn, 4.0 * B * d.T * double(d.D), double(B) * d.T * 2 * d.D * 2.0, s);
+    SV_TRY(map_attn_launch(m.qv, m.KV, m.a, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, s));
+  }
+  e.bias = g_w.mo_b;
+  e.out = m.A;
+  SV_TRY(run_gemm(m.out, e, d.D, s));
+  {
+    Launch L(kKindLN, 8.0 * B * d.D, double(B) * d.D * 3.0, s);
+    SV_TRY(layernorm_launch(m.A, g_w.mln_g, g_w.mln_b, m.Ya, B, d.D, 1e-6f, fp8, s));
+  }
+  e.bias = g_w.mfc1_b;
+  e.act = SV_ACT_GELU_TANH;
+  e.out_e4m3 = fp8;
+  e.out = m.Ha;
+  SV_TRY(run_gemm(m.fc1, e, d.D, s));
+  e.bias = g_w.mfc2_b;
+  e.act = SV_ACT_NONE;
+  e.out_e4m3 = 0;
+  e.residual = m.A;
+  e.out = out;
+  return run_gemm(m.fc2, e, d.F, s);
+}
+
+sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStream_t s) {
+  const Dims& d = g_w.d;
+  const int B = p.B, fp8 = p.fp8;
+  const int M = B * d.T;
+  const float sc = fp8 ? 1.0f / 256.0f : 1.0f;
+  {
+    Launch L(kKindOther, 0.0, double(M) * (d.P * 2.0 + d.Kp * (fp8 ? 1.0 : 2.0)), s);
+    SV_TRY(pad_pixels_launch(pixels, p.A0, M, d.P, d.Kp, fp8, s));
+  }
+  GemmEpi e;
+  e.scale = sc;
+  e.bias = g_w.patch_b;
+  e.pos = g_w.pos;
+  e.pos_rows = d.T;
+  e.out = p.X;
+  SV_TRY(run_gemm(p.patch, e, d.P, s));
+  for (int l = 0; l < layers; ++l) {
+    const LayerW& w = g_w.layers[size_t(l)];
+    SV_TRY(run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
+    GemmEpi q;
+    q.scale = sc;
+    q.bias = w.qkv_b;
+    q.out = p.QKV;
+    SV_TRY(run_gemm(p.qkv[size_t(l)], q, d.D, s));
+    {
+      Launch L(kKindAttn, 4.0 * B * d.H * double(d.T) * double(d.T) * 72.0,
+               double(M) * 3 * d.D * 2.0 + double(M) * d.D * (fp8 ? 1.0 : 2.0), s);
+      SV_TRY(attention_launch(p.attn, p.O, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, s));
+    }
+    GemmEpi o;
+    o.scale = sc;
+    o.bias = w.out_b;
+    o.residual = p.X;
+    o.out = p.X;
+    SV_TRY(run_gemm(p.out[size_t(l)], o, d.D, s));
+    SV_TRY(run_ln(p.X, w.ln2_g, w.ln2_b, p.Y, M, fp8, s));
+    GemmEpi f1;
+    f1.scale = sc;
+    f1.bias = w.fc1_b;
+    f1.act = SV_ACT_GELU_TANH;
+    f1.out_e4m3 = fp8;
+    f1.out = p.Hh;
+    SV_TRY(run_gemm(p.fc1[size_t(l)], f1, d.D, s));
+    GemmEpi f2;
+    f2.scale = sc;
+    f2.bias = w.fc2_b;
+    f2.residual = p.X;
+    f2.out = p.X;
+    SV_TRY(run_gemm(p.fc2[size_t(l)], f2, d.F, s));
+  }
+  SV_TRY(run_ln(p.X, g_w.enc_ln_g, g_w.enc_ln_b, p.Y, M, fp8, s));
+  return run_map(p.map, B, fp8, out, s);
+}
+
+sv_status check_ready() {
+  if (!g_w.ready) {
+    set_error("weights are not initialised: call sv_init_weights first");
+    return SV_ERR_NOT_INITIALIZED;
+  }
+  return SV_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ shared helpers
+void set_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+}
+
+sv_status cuda_fail(cudaError_t e, const char* what) {
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return e == cudaErrorMemoryAllocation ? SV_ERR_OOM : SV_ERR_CUDA;
+}
+
+sv_status ensure_runtime() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (g_rt.ready && g_rt.device == dev) return SV_OK;
+  if (g_rt.ready && g_rt.device != dev) {
+    set_error("the library was initialised on device %d; device %d is current", g_rt.device, dev);
+    return SV_ERR_INVALID_ARG;
+  }
+  int sms = 0, major = 0, minor = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) {
+    set_error("this library is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+    return SV_ERR_UNSUPPORTED;
+  }
+  int* err = nullptr;
+  e = cudaMalloc(&err, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+  e = cudaMemset(err, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+  g_rt.device = dev;
+  g_rt.sms = sms;
+  g_rt.dev_err = err;
+  g_rt.ready = true;
+  return SV_OK;
+}
+
+int* dev_err() { return g_rt.dev_err; }
+int num_sms() { return g_rt.sms; }
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+sv_status sv_init_weights(uint64_t seed) { return sv_init_weights_dims(seed, 729, 588, 1152, 16, 4304, 27); }
+
+sv_status sv_init_weights_dims(uint64_t seed, int tokens, int patch_dim, int width, int heads, int mlp, int layers) {
+  if (tokens < 1 || patch_dim < 1 || patch_dim > 4096 || heads < 1 || layers < 1 || layers > 64 || mlp < 16) {
+    set_error("sv_init_weights_dims: sizes out of range");
+    return SV_ERR_INVALID_ARG;
+  }
+  if (width != heads * 72 || width % 16 != 0 || mlp % 16 != 0 || patch_dim % 4 != 0 || width > 4096) {
+    set_error("sv_init_weights_dims: needs width == heads*72, width %% 16 == 0, mlp %% 16 == 0, patch_dim %% 4 == 0");
+    return SV_ERR_UNSUPPORTED;
+  }
+  Dims d;
+  d.T = tokens;
+  d.P = patch_dim;
+  d.D = width;
+  d.H = heads;
+  d.F = mlp;
+  d.L = layers;
+  d.Kp = int(align_up(size_t(patch_dim), 16));
+  return init_weights(seed, d);
+}
+
+sv_status sv_model_dims(int* tokens, int* patch_dim, int* width, int* heads, int* mlp, int* layers) {
+  SV_TRY(check_ready());
+  const Dims& d = g_w.d;
+  if (tokens) *tokens = d.T;
+  if (patch_dim) *patch_dim = d.P;
+  if (width) *width = d.D;
+  if (heads) *heads = d.H;
+  if (mlp) *mlp = d.F;
+  if (layers) *layers = d.L;
+  return SV_OK;
+}
+
+sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int gemm_dtype, void* stream) {
+  SV_TRY(check_ready());
+  if (!pixels || !out || batch < 1 || layers < 1 || layers > g_w.d.L ||
+      (gemm_dtype != SV_GEMM_F16 && gemm_dtype != SV_GEMM_E4M3)) {
+    set_error("sv_encode: bad arguments (batch %d, layers %d of %d, gemm_dtype %d)", batch, layers, g_w.d.L,
+              gemm_dtype);
+    return SV_ERR_INVALID_ARG;
+  }
+  if (!aligned(pixels, 8) || !aligned(out, 16)) {
+    set_error("sv_encode: pixels must be 8-byte and out 16-byte aligned");
+    return SV_ERR_INVALID_ARG;
+  }
+  if (long(batch) * g_w.d.T > (1L << 30)) {
+    set_error("sv_encode: batch too large");
+    return SV_ERR_INVALID_ARG;
+  }
+  Plan* p = nullptr;
+  SV_TRY(get_plan(batch, gemm_dtype, &p));
+  return encode(*p, static_cast<const __half*>(pixels), static_cast<__half*>(out), layers,
+                static_cast<cudaStream_t>(stream));
+}
+
+sv_status sv_gemm_bias_act(const void* A, const void* W, const void* bias, const void* pos, int pos_rows,
+                           const void* residual, void* C, int M, int N, int K, int act, int in_dtype, int out_dtype,
+                           float scale, void* stream) {
+  if (!A || !W || !C || M < 1 || N < 16 || K < 16 || N % 16 || K % 16 || (act != 0 && act != 1) ||
+      (in_dtype != 0 && in_dtype != 1) || (out_dtype != 0 && out_dtype != 1) || (pos && pos_rows < 1) ||
+      !std::isfinite(scale)) {
+    set_error("sv_gemm_bias_act: bad arguments (M %d N %d K %d; N and K must be multiples of 16)", M, N, K);
+    return SV_ERR_INVALID_ARG;
+  }
+  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16) || !aligned(bias, 16) || !aligned(pos, 16) ||
+      !aligned(residual, 16)) {
+    set_error("sv_gemm_bias_act: all pointers must be 16-byte aligned");
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_TRY(ensure_runtime());
+  GemmOperands g;
+  SV_TRY(gemm_prepare(&g, A, W, M, N, K, in_dtype));
+  GemmEpi e;
+  e.bias = static_cast<const __half*>(bias);
+  e.pos = static_cast<const __half*>(pos);
+  e.pos_rows = pos_rows;
+  e.residual = static_cast<const __half*>(residual);
+  e.out = C;
+  e.act = act;
+  e.out_e4m3 = out_dtype;
+  e.scale = scale;
+  return run_gemm(g, e, K, static_cast<cudaStream_t>(stream));
+}
+
+sv_status sv_layernorm(const void* x, const void* gamma, const void* beta, void* y, int rows, int width, float eps,
+                       int out_dtype, void* stream) {
+  if (!x || !gamma || !beta || !y || rows < 1 || width < 8 || width > 4096 || width % 8 || !(eps >= 0.0f) ||
+      (out_dtype != 0 && out_dtype != 1)) {
+    set_error("sv_layernorm: bad arguments (rows %d, width %d)", rows, width);
+    return SV_ERR_INVALID_ARG;
+  }
+  if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(beta, 16) || !aligned(y, 16)) {
+    set_error("sv_layernorm: pointers must be 16-byte aligned");
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_TRY(ensure_runtime());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch L(kKindLN, 8.0 * rows * width, double(rows) * width * (2.0 + (out_dtype ? 1.0 : 2.0)), s);
+  return layernorm_launch(static_cast<const __half*>(x), static_cast<const __half*>(gamma),
+                          static_cast<const __half*>(beta), y, rows, width, eps, out_dtype, s);
+}
+
+sv_status sv_attention(const void* qkv, void* o, int batch, int heads, int tokens, int head_dim, float scale,
+                       int out_dtype, void* stream) {
+  if (!qkv || !o || batch < 1 || heads < 1 || tokens < 1 || batch > 65535 || !std::isfinite(scale) ||
+      (out_dtype != 0 && out_dtype != 1)) {
+    set_error("sv_attention: bad arguments");
+    return SV_ERR_INVALID_ARG;
+  }
+  if (head_dim != 72) {
+    set_error("sv_attention: head_dim %d is not supported (72 only)", head_dim);
+    return SV_ERR_UNSUPPORTED;
+  }
+  if (!aligned(qkv, 16) || !aligned(o, 16)) {
+    set_error("sv_attention: pointers must be 16-byte aligned");
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_TRY(ensure_runtime());
+  CUtensorMap m;
+  SV_TRY(attention_map(&m, qkv, batch, tokens, heads));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch L(kKindAttn, 4.0 * batch * heads * double(tokens) * tokens * 72.0, 0.0, s);
+  return attention_launch(m, o, batch, tokens, heads, scale, out_dtype, s);
+}
+
+sv_status sv_map_pool(const void* x, void* out, int batch, int gemm_dtype, void* stream) {
+  SV_TRY(check_ready());
+  if (!x || !out || batch < 1 || (gemm_dtype != 0 && gemm_dtype != 1)) {
+    set_error("sv_map_pool: bad arguments");
+    return SV_ERR_INVALID_ARG;
+  }
+  if (!aligned(x, 16) || !aligned(out, 16)) {
+    set_error("sv_map_pool: pointers must be 16-byte aligned");
+    return SV_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Dims& d = g_w.d;
+  const int fp8 = gemm_dtype;
+  const auto key = std::make_pair(batch, fp8);
+  auto it = g_map_plans.find(key);
+  Plan* p = nullptr;
+  if (it == g_map_plans.end()) {
+    std::unique_ptr<Plan> np(new Plan());
+    np->B = batch;
+    np->fp8 = fp8;
+    Carver c{nullptr};
+    for (int pass = 0; pass < 2; ++pass) {
+      np->Y = fp8 ? c.take(size_t(batch) * d.T * d.D) : nullptr;  // quantised copy of x
+      if (c.base && !fp8) np->Y = const_cast<void*>(x);
+      SV_TRY(build_map(np->map, c, np->Y ? np->Y : x, batch, fp8, true, nullptr));
+      if (pass == 0) SV_TRY(alloc_carved(c, &np->mem, &np->bytes));
+    }
+    p = np.get();
+    g_map_plans[key] = std::move(np);
+  } else {
+    p = it->second.get();
+    if (!fp8 && p->Y != x) {  // the KV operand map follows the caller's buffer
+      SV_TRY(gemm_prepare(&p->map.kv, x, g_w.mkv_w, batch * d.T, 2 * d.D, d.D, 0));
+      p->Y = const_cast<void*>(x);
+    }
+  }
+  if (fp8) {
+    Launch L(kKindOther, 0.0, double(batch) * d.T * d.D * 3.0, s);
+    SV_TRY(quantize_launch(static_cast<const __half*>(x), static_cast<uint8_t*>(p->Y), size_t(batch) * d.T * d.D, s));
+  }
+  return run_map(p->map, batch, fp8, static_cast<__half*>(out), s);
+}
+
+sv_status sv_quantize_e4m3(const void* x, void* y, size_t n, void* stream) {
+  if (!x || !y || n % 16 || !aligned(x, 16) || !aligned(y, 16)) {
+    set_error("sv_quantize_e4m3: needs n %% 16 == 0 and 16-byte aligned pointers");
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_TRY(ensure_runtime());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch L(kKindOther, 0.0, double(n) * 3.0, s);
+  return quantize_launch(static_cast<const __half*>(x), static_cast<uint8_t*>(y), n, s);
+}
+
+sv_status sv_make_pixels(uint64_t seed, int batch, void* dev_dst, void* stream) {
+  SV_TRY(check_ready());
+  if (!dev_dst || batch < 1) {
+    set_error("sv_make_pixels: bad arguments");
+    return SV_ERR_INVALID_ARG;
+  }
+  const Dims& d = g_w.d;
+  std::vector<uint16_t> host(size_t(batch) * d.T * d.P);
+  synth_pixels_f16(seed, batch, d.T, d.P, host.data());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SV_CHECK_CUDA(cudaMemcpyAsync(dev_dst, host.data(), host.size() * 2, cudaMemcpyHostToDevice, s), "pixel upload");
+  SV_CHECK_CUDA(cudaStreamSynchronize(s), "pixel upload");
+  return SV_OK;
+}
+
+sv_status sv_sync(void* stream) {
+  SV_TRY(ensure_runtime());
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sv_sync");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "sv_sync (pending error)");
+  int flag = 0;
+  e = cudaMemcpy(&flag, g_rt.dev_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "sv_sync (error word)");
+  if (flag) {
+    cudaMemset(g_rt.dev_err, 0, sizeof(int));
+    set_error("a kernel gave up a bounded wait (device error word 0x%x); its outputs are undefined", flag);
+    return SV_ERR_TIMEOUT;
+  }
+  return SV_OK;
+}
+
+const char* sv_last_error(void) { return g_err.c_str(); }
+
+long long sv_launch_count(void) {
+  const long long n = g_launches;
+  g_launches = 0;
+  return n;
+}
+
+sv_status sv_profile_enable(int on) {
+  g_prof_on = on != 0;
+  return SV_OK;
+}
+
+sv_status sv_profile_read(int kind, double* ms, double* flops, double* bytes, long long* launches) {
+  if (kind < 0 || kind >= kNumKinds) {
+    set_error("sv_profile_read: kind %d out of range", kind);
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_CHECK_CUDA(cudaDeviceSynchronize(), "sv_profile_read");
+  double t = 0, f = 0, b = 0;
+  long long n = 0;
+  std::vector<ProfRec> keep;
+  for (const ProfRec& r : g_prof) {
+    if (r.kind != kind) {
+      keep.push_back(r);
+      continue;
+    }
+    float x = 0;
+    cudaEventElapsedTime(&x, r.e0, r.e1);
+    t += x;
+    f += r.flops;
+    b += r.bytes;
+    ++n;
+    g_ev_pool.push_back(r.e0);
+    g_ev_pool.push_back(r.e1);
+  }
+  g_prof.swap(keep);
+  if (ms) *ms = t;
+  if (flops) *flops = f;
+  if (bytes) *bytes = b;
+  if (launches) *launches = n;
+  return SV_OK;
+}
+
+sv_status sv_debug_fill_workspace(int batch, int gemm_dtype, int byte_value) {
+  SV_TRY(check_ready());
+  if (batch < 1 || (gemm_dtype != 0 && gemm_dtype != 1)) {
+    set_error("sv_debug_fill_workspace: bad arguments");
+    return SV_ERR_INVALID_ARG;
+  }
+  Plan* p = nullptr;
+  SV_TRY(get_plan(batch, gemm_dtype, &p));
+  SV_CHECK_CUDA(cudaMemset(p->mem, byte_value & 0xFF, p->bytes), "sv_debug_fill_workspace");
+  SV_CHECK_CUDA(cudaDeviceSynchronize(), "sv_debug_fill_workspace");
+  return SV_OK;
+}
+
+sv_status sv_debug_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 2000000u) {
+    set_error("sv_debug_wait_timeout: limit must be in 1..2000000 us");
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_TRY(ensure_runtime());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch L(kKindOther, 0.0, 0.0, s);
+  return wait_probe_launch(limit_us, s);
+}
+
+void sv_shutdown(void) {
+  if (g_rt.ready) cudaDeviceSynchronize();
+  free_weights();
+  for (const ProfRec& r : g_prof) {
+    cudaEventDestroy(r.e0);
+    cudaEventDestroy(r.e1);
+  }
+  g_prof.clear();
+  for (cudaEvent_t e : g_ev_pool) cudaEventDestroy(e);
+  g_ev_pool.clear();
+  if (g_rt.dev_err) cudaFree(g_rt.dev_err);
+  g_rt = Runtime();
+}
+
+}  // extern "C"

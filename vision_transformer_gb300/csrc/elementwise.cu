@@ -1,0 +1,297 @@
+// Memory-bound kernels: LayerNorm, pixel staging, E4M3 quantisation and the
+// single-query MAP attention, plus the bounded-wait self-test kernel.
+#include <cuda_fp8.h>
+
+#include "ptx.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * a, 16.0f * b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * c, 16.0f * d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+// LayerNorm, one warp per row ("SigLIP ViT benchmark", LayerNorm paragraph):
+// mean, then the centred (biased) variance, both in F32 from the row held in
+// registers, then the affine map. Each lane owns CPL chunks of 4 values
+// (8-byte loads); a 1152-wide row is 9 chunks per lane.
+template <int CPL>
+__global__ void __launch_bounds__(256) layernorm_kernel(const __half* __restrict__ x, const __half* __restrict__ g,
+                                                        const __half* __restrict__ bta, void* __restrict__ y,
+                                                        int rows, int width, float eps, int out_e4m3) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long row = long(blockIdx.x) * 8 + warp;
+  if (row >= rows) return;
+  const int chunks = width >> 2;
+  const __half* xr = x + row * long(width);
+  float v[CPL][4];
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = lane + 32 * i;
+    if (c < chunks) {
+      const uint2 u = *reinterpret_cast<const uint2*>(xr + 4 * c);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      v[i][0] = a.x;
+      v[i][1] = a.y;
+      v[i][2] = b.x;
+      v[i][3] = b.y;
+      s += (a.x + a.y) + (b.x + b.y);
+    } else {
+      v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.0f;
+    }
+  }
+  const float mean = warp_sum(s) / float(width);
+  float q = 0.0f;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i)
+    if (lane + 32 * i < chunks) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float d = v[i][k] - mean;
+        q = fmaf(d, d, q);
+      }
+    }
+  const float var = warp_sum(q) / float(width);
+  const float rstd = rsqrtf(var + eps);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = lane + 32 * i;
+    if (c < chunks) {
+      const uint2 gu = __ldg(reinterpret_cast<const uint2*>(g + 4 * c));
+      const uint2 bu = __ldg(reinterpret_cast<const uint2*>(bta + 4 * c));
+      const float2 g0 = __half22float2(*reinterpret_cast<const __half2*>(&gu.x));
+      const float2 g1 = __half22float2(*reinterpret_cast<const __half2*>(&gu.y));
+      const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&bu.x));
+      const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&bu.y));
+      const float o0 = fmaf((v[i][0] - mean) * rstd, g0.x, b0.x);
+      const float o1 = fmaf((v[i][1] - mean) * rstd, g0.y, b0.y);
+      const float o2 = fmaf((v[i][2] - mean) * rstd, g1.x, b1.x);
+      const float o3 = fmaf((v[i][3] - mean) * rstd, g1.y, b1.y);
+      if (!out_e4m3) {
+        uint2 w;
+        *reinterpret_cast<__half2*>(&w.x) = __floats2half2_rn(o0, o1);
+        *reinterpret_cast<__half2*>(&w.y) = __floats2half2_rn(o2, o3);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(y) + row * long(width) + 4 * c) = w;
+      } else {
+        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(y) + row * long(width) + 4 * c) = e4m3x4(o0, o1, o2, o3);
+      }
+    }
+  }
+}
+
+// Pixels [rows, P] f16 -> GEMM operand [rows, Kp] (f16 or e4m3 codes), zero
+// columns P..Kp-1 (the K tail both GEMM operands share). One thread per 4 values.
+__global__ void pad_pixels_kernel(const __half* __restrict__ pix, void* __restrict__ out, long rows, int P, int Kp,
+                                  int out_e4m3) {
+  const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int cpr = Kp >> 2;
+  if (i >= rows * cpr) return;
+  const long row = i / cpr;
+  const int c = int(i % cpr) * 4;
+  uint2 u = make_uint2(0, 0);
+  if (c < P) u = *reinterpret_cast<const uint2*>(pix + row * long(P) + c);
+  if (!out_e4m3) {
+    *reinterpret_cast<uint2*>(static_cast<__half*>(out) + row * long(Kp) + c) = u;
+  } else {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(out) + row * long(Kp) + c) = e4m3x4(a.x, a.y, b.x, b.y);
+  }
+}
+
+// y = e4m3 code of 16 x, 16 values per thread.
+__global__ void quantize_kernel(const __half* __restrict__ x, uint8_t* __restrict__ y, size_t n16) {
+  const size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n16) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x) + 2 * i;
+  uint4 w;
+  uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 u = src[h];
+    const __half2* hp = reinterpret_cast<const __half2*>(&u);
+    const float2 a = __half22float2(hp[0]), b = __half22float2(hp[1]);
+    const float2 c = __half22float2(hp[2]), d = __half22float2(hp[3]);
+    wp[2 * h] = e4m3x4(a.x, a.y, b.x, b.y);
+    wp[2 * h + 1] = e4m3x4(c.x, c.y, d.x, d.y);
+  }
+  reinterpret_cast<uint4*>(y)[i] = w;
+}
+
+// MAP attention: one learned query per head over the T tokens of one image
+// ("SigLIP ViT benchmark": the probe's cross-attention). q: [D] f16 (the
+// projected probe, shared by every image); kv: [B*T, 2D] f16 (K | V).
+// One CTA of 128 threads per (head, image); scores and the F32 softmax in
+// shared memory; the weighted V sum split over 14 key groups x 9 column groups.
+constexpr int kMapThreads = 128;
+constexpr int kMapKeyGroups = 14;
+
+__global__ void __launch_bounds__(kMapThreads) map_attn_kernel(const __half* __restrict__ q,
+                                                               const __half* __restrict__ kv, void* __restrict__ out,
+                                                               int T, int D, float scale_log2, int out_e4m3) {
+  extern __shared__ float sm[];
+  float* s = sm;        // [T]
+  float* red = sm + T;  // [kMapKeyGroups][72]
+  __shared__ float qf[72];
+  __shared__ float wred[4];
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 72) qf[tid] = __half2float(q[h * 72 + tid]);
+  __syncthreads();
+  const size_t ld = size_t(2) * size_t(D);
+  const __half* base = kv + size_t(b) * size_t(T) * ld;
+  float mx = -INFINITY;
+  for (int t = tid; t < T; t += kMapThreads) {
+    const uint4* kr = reinterpret_cast<const uint4*>(base + size_t(t) * ld + size_t(h) * 72);
+    float dot = 0.0f;
+#pragma unroll
+    for (int g = 0; g < 9; ++g) {
+      const uint4 u = __ldg(kr + g);
+      const __half2* hp = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(hp[i]);
+        dot = fmaf(f.x, qf[8 * g + 2 * i], dot);
+        dot = fmaf(f.y, qf[8 * g + 2 * i + 1], dot);
+      }
+    }
+    s[t] = dot * scale_log2;
+    mx = fmaxf(mx, s[t]);
+  }
+  mx = warp_max(mx);
+  if (lane == 0) wred[warp] = mx;
+  __syncthreads();
+  mx = fmaxf(fmaxf(wred[0], wred[1]), fmaxf(wred[2], wred[3]));
+  __syncthreads();
+  float sum = 0.0f;
+  for (int t = tid; t < T; t += kMapThreads) {
+    const float pv = ex2(s[t] - mx);
+    s[t] = pv;
+    sum += pv;
+  }
+  sum = warp_sum(sum);
+  if (lane == 0) wred[warp] = sum;
+  __syncthreads();
+  const float l = (wred[0] + wred[1]) + (wred[2] + wred[3]);
+  const int grp = tid / 9, cg = tid % 9;
+  if (grp < kMapKeyGroups) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int t = grp; t < T; t += kMapKeyGroups) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(base + size_t(t) * ld + size_t(D) + size_t(h) * 72) + cg);
+      const __half2* hp = reinterpret_cast<const __half2*>(&u);
+      const float pt = s[t];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(hp[i]);
+        acc[2 * i] = fmaf(pt, f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(pt, f.y, acc[2 * i + 1]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[grp * 72 + cg * 8 + i] = acc[i];
+  }
+  __syncthreads();
+  if (tid < 72) {
+    float a = 0.0f;
+    for (int g2 = 0; g2 < kMapKeyGroups; ++g2) a += red[g2 * 72 + tid];
+    a /= l;
+    const size_t o = size_t(b) * size_t(D) + size_t(h) * 72 + tid;
+    if (!out_e4m3)
+      static_cast<__half*>(out)[o] = __float2half_rn(a);
+    else
+      static_cast<uint8_t*>(out)[o] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(16.0f * a, __NV_SATFINITE, __NV_E4M3));
+  }
+}
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// completes; the wait gives up after limit_ns, sets the device error word and
+// the kernel returns normally.
+__global__ void wait_probe_kernel(unsigned long long limit_ns, int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+    mbar_arrive(smem_u32(&bar));  // completes the phase so the barrier is left consistent
+  }
+}
+
+template <int CPL>
+void ln_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width, float eps,
+               int out_e4m3, cudaStream_t s) {
+  layernorm_kernel<CPL><<<(rows + 7) / 8, 256, 0, s>>>(x, g, b, y, rows, width, eps, out_e4m3);
+}
+
+}  // namespace
+
+sv_status layernorm_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width,
+                           float eps, int out_e4m3, cudaStream_t s) {
+  const int cpl = (width / 4 + 31) / 32;
+  if (cpl <= 1) ln_launch<1>(x, g, b, y, rows, width, eps, out_e4m3, s);
+  else if (cpl <= 2) ln_launch<2>(x, g, b, y, rows, width, eps, out_e4m3, s);
+  else if (cpl <= 4) ln_launch<4>(x, g, b, y, rows, width, eps, out_e4m3, s);
+  else if (cpl <= 9) ln_launch<9>(x, g, b, y, rows, width, eps, out_e4m3, s);
+  else if (cpl <= 16) ln_launch<16>(x, g, b, y, rows, width, eps, out_e4m3, s);
+  else if (cpl <= 32) ln_launch<32>(x, g, b, y, rows, width, eps, out_e4m3, s);
+  else {
+    set_error("layernorm: width %d too large", width);
+    return SV_ERR_UNSUPPORTED;
+  }
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "layernorm launch");
+}
+
+sv_status pad_pixels_launch(const __half* pix, void* out, long rows, int P, int Kp, int out_e4m3, cudaStream_t s) {
+  const long n = rows * (Kp / 4);
+  pad_pixels_kernel<<<unsigned((n + 255) / 256), 256, 0, s>>>(pix, out, rows, P, Kp, out_e4m3);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "pad_pixels launch");
+}
+
+sv_status quantize_launch(const __half* x, uint8_t* y, size_t n, cudaStream_t s) {
+  const size_t n16 = n / 16;
+  if (n16 == 0) return SV_OK;
+  quantize_kernel<<<unsigned((n16 + 255) / 256), 256, 0, s>>>(x, y, n16);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "quantize launch");
+}
+
+sv_status wait_probe_launch(unsigned int limit_us, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(1000ull * limit_us, dev_err());
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "wait probe launch");
+}
+
+sv_status map_attn_launch(const __half* q, const __half* kv, void* out, int B, int T, int H, float scale,
+                          int out_e4m3, cudaStream_t s) {
+  const size_t smem = sizeof(float) * (size_t(T) + size_t(kMapKeyGroups) * 72);
+  static size_t attr = 0;
+  if (smem > 48 * 1024 && smem > attr) {
+    cudaError_t e = cudaFuncSetAttribute(map_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(map_attn)");
+    attr = smem;
+  }
+  map_attn_kernel<<<dim3(H, B), kMapThreads, smem, s>>>(q, kv, out, T, H * 72, scale * 1.4426950408889634f,
+                                                         out_e4m3);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "map_attn launch");
+}
+
+}  // namespace sv

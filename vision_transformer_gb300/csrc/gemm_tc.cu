@@ -1,0 +1,435 @@
+// Dense projection GEMM on the 5th-generation tensor cores (tcgen05 + TMEM),
+// with the epilogues of the encoder fused in: bias, positional embedding,
+// tanh-GELU, residual add, F16 or E4M3 output.
+//
+// C[M,N] = epi(A[M,K] . W[N,K]^T): every dense GEMM of the encoder ("SigLIP
+// ViT benchmark": the 588->1152 patch embedding, the fused 1152->3456 QKV
+// projection, the output projection, the 1152->4304->1152 MLP, and the MAP
+// head's Q, KV, output and MLP projections).
+//
+// Design (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A and W tiles (128-byte swizzled, 128 bytes of
+//               K per stage) into a ring of shared-memory stages;
+//   warp 1      allocates TMEM and issues tcgen05.mma (M = 128, N = BN) from
+//               one thread; the accumulator (F32) lives in TMEM, double
+//               buffered so the epilogue of one tile overlaps the next tile's
+//               main loop;
+//   warps 2..5  epilogue: tcgen05.ld of 32 columns at a time, fused math,
+//               16-byte global stores.
+// F16 operands use kind::f16 (K = 16 per instruction); E4M3 operands use
+// kind::f8f6f4 (K = 32 per instruction) with the dequantisation scale
+// applied to the accumulator. All waits are bounded (ptx.cuh).
+#include <cuda_fp8.h>
+
+#include <cstdio>
+
+#include "ptx.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBKBytes = 128;  // K bytes per stage: one 128-byte swizzle row
+constexpr int kThreads = 192;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStageA = kBM * kBKBytes;
+  static constexpr int kStageB = BN * kBKBytes;
+  static constexpr int kStage = kStageA + kStageB;
+  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 192 ? 5 : (BN >= 128 ? 6 : 8));
+  static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes;
+  static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+struct Params {
+  int M, N, K;
+  int m_tiles, n_tiles, k_blocks;
+  const __half* bias;
+  const __half* pos;
+  int pos_rows;
+  const __half* residual;
+  void* out;
+  int act, out_e4m3;
+  float scale;
+  int* err;
+};
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+  // 0.5 x (1 + tanh(u)) == x / (1 + exp(-2u)),  u = sqrt(2/pi) (x + 0.044715 x^3)
+  const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+  return __fdividef(x, 1.0f + __expf(-2.0f * u));
+}
+
+__device__ __forceinline__ void load8h(const __half* p, float* f) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// Epilogue for 32 consecutive columns [n, n+32) of one row (n < N, N % 16 == 0).
+__device__ __forceinline__ void epilogue32(const Params& p, int row, int n, const uint32_t (&r)[32]) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * p.scale;
+  const int ngroups = min(4, (p.N - n) / 8);  // valid groups of 8 columns
+  const size_t rowoff = size_t(row) * size_t(p.N) + size_t(n);
+  if (p.bias) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (g < ngroups) {
+        float b[8];
+        load8h(p.bias + n + 8 * g, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * g + i] += b[i];
+      }
+  }
+  if (p.pos) {
+    const size_t poff = size_t(row % p.pos_rows) * size_t(p.N) + size_t(n);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (g < ngroups) {
+        float b[8];
+        load8h(p.pos + poff + 8 * g, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * g + i] += b[i];
+      }
+  }
+  if (p.act == SV_ACT_GELU_TANH) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+  }
+  if (p.residual) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (g < ngroups) {
+        float b[8];
+        load8h(p.residual + rowoff + 8 * g, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * g + i] += b[i];
+      }
+  }
+  if (!p.out_e4m3) {
+    __half* o = static_cast<__half*>(p.out) + rowoff;
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (g < ngroups) {
+        uint4 w;
+        __half2* h = reinterpret_cast<__half2*>(&w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[8 * g + 2 * i], v[8 * g + 2 * i + 1]);
+        *reinterpret_cast<uint4*>(o + 8 * g) = w;
+      }
+  } else {
+    uint8_t* o = static_cast<uint8_t*>(p.out) + rowoff;
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+      if (2 * g < ngroups) {  // N % 16 == 0: groups of 16 bytes are whole
+        uint4 w;
+        __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          q[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * v[16 * g + 2 * i], 16.0f * v[16 * g + 2 * i + 1]),
+                                          __NV_SATFINITE, __NV_E4M3);
+        *reinterpret_cast<uint4*>(o + 16 * g) = w;
+      }
+  }
+}
+
+template <int BN, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const Params p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar_full = smem_u32(bars);
+  const uint32_t bar_empty = bar_full + 8 * C::kStages;
+  const uint32_t bar_tfull = bar_empty + 8 * C::kStages;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_drain = bar_tempty + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, 128);  // every epilogue thread arrives
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_tiles = p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_phase = 0;  // stages with loads in flight, and their phase bit
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          mbar_arrive_expect_tx(fb, C::kStage);
+          const uint32_t sa = smem_u32(smem + stage * C::kStage);
+          const int kc = kb * (FP8 ? 128 : 64);
+          tma_load_2d(sa, &tmA, fb, kc, mt * kBM);
+          tma_load_2d(sa + C::kStageA, &tmW, fb, kc, nt * BN);
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Every copy this thread issued lands before the CTA can exit (immediate
+      // on the normal path, where the MMA warp already consumed them all).
+      for (int st = 0; st < C::kStages; ++st)
+        if (issued & (1u << st)) mbar_wait_bounded(bar_full + 8 * st, (issued_phase >> st) & 1, p.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(kBM, BN, 0, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::kStage);
+          const uint32_t sb = sa + C::kStageA;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // 4 instructions x 32 bytes of K
+            const uint64_t ad = make_sdesc(sa + 32 * j, 16, 1024, 2);
+            const uint64_t bd = make_sdesc(sb + 32 * j, 16, 1024, 2);
+            const uint32_t accum = (kb | j) != 0;
+            if (FP8)
+              mma_f8(d, ad, bd, idesc, accum);
+            else
+              mma_f16(d, ad, bd, idesc, accum);
+          }
+          tc_commit(bar_empty + 8 * stage);  // frees the stage when these MMAs finish
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) tc_commit(bar_tfull + 8 * acc);
+      }
+      // All MMAs this thread issued complete before TMEM is released.
+      tc_commit(bar_drain);
+      mbar_wait_bounded(bar_drain, 0, p.err);
+    }
+  } else {
+    const int sub = warp & 3;  // TMEM lanes 32*sub .. 32*sub+31
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int row = mt * kBM + sub * 32 + lane;
+      const int n0 = nt * BN;
+      const uint32_t tbase = tmem_base + uint32_t(acc * BN) + (uint32_t(sub * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int n = n0 + 32 * c;
+        if (n >= p.N) break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld32(tbase + 32 * c, r);
+        tmem_ld_wait();
+        if (row < p.M) epilogue32(p, row, n, r);
+      }
+      tc_fence_before();
+      mbar_arrive(bar_tempty + 8 * acc);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int BN, bool FP8>
+sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
+  using C = Cfg<BN>;
+  static bool attr_set = false;
+  auto kern = gemm_tc_kernel<BN, FP8>;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm)");
+    attr_set = true;
+  }
+  const int tiles = prm.m_tiles * prm.n_tiles;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  kern<<<grid, kThreads, C::kSmem, s>>>(g.ta, g.tw, prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+  return SV_OK;
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+sv_status make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
+  EncodeFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return SV_ERR_CUDA;
+  }
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) gs[i] = strides_bytes[i];
+  }
+  CUresult r = fn(m, dt, cuuint32_t(rank), const_cast<void*>(ptr), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d): rank %d dims0 %llu dims1 %llu box %u x %u", int(r), rank,
+              (unsigned long long)dims[0], (unsigned long long)(rank > 1 ? dims[1] : 0), box[0],
+              rank > 1 ? box[1] : 0);
+    return SV_ERR_INVALID_ARG;
+  }
+  return SV_OK;
+}
+
+sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int fp8, int box_rows) {
+  const uint64_t dims[2] = {uint64_t(K), uint64_t(rows)};
+  const uint64_t strides[1] = {uint64_t(K) * (fp8 ? 1u : 2u)};
+  const uint32_t box[2] = {uint32_t(fp8 ? 128 : 64), uint32_t(box_rows)};
+  return make_tmap(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, dims, strides,
+                   box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output-tile width: estimated main-loop time = waves x per-tile time, where a
+// tile's K-step costs max(tensor time, shared-memory operand traffic / 128 B per clock).
+int gemm_pick_bn(int M, int N, int K) {
+  const int cand[4] = {256, 192, 128, 64};
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  int best = 256;
+  double best_t = 1e30;
+  const int mt = (M + kBM - 1) / kBM;
+  for (int bn : cand) {
+    const double mma = bn / 2.0;
+    const double smem = (kBM * 32.0 + bn * 32.0) / 128.0;
+    const double step = mma > smem ? mma : smem;
+    const long tiles = long(mt) * ((N + bn - 1) / bn);
+    const long waves = (tiles + sms - 1) / sms;
+    const double t = double(waves) * step * double((K + 15) / 16);
+    if (t < best_t * 0.999) {
+      best_t = t;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8) {
+  g->M = M;
+  g->N = N;
+  g->K = K;
+  g->fp8 = fp8;
+  g->bn = gemm_pick_bn(M, N, K);
+  sv_status st = gemm_operand_map(&g->ta, A, M, K, fp8, kBM);
+  if (st != SV_OK) return st;
+  return gemm_operand_map(&g->tw, W, N, K, fp8, g->bn);
+}
+
+sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
+  Params p;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.m_tiles = (g.M + kBM - 1) / kBM;
+  p.n_tiles = (g.N + g.bn - 1) / g.bn;
+  const int bk = g.fp8 ? 128 : 64;
+  p.k_blocks = (g.K + bk - 1) / bk;
+  p.bias = e.bias;
+  p.pos = e.pos;
+  p.pos_rows = e.pos_rows > 0 ? e.pos_rows : 1;
+  p.residual = e.residual;
+  p.out = e.out;
+  p.act = e.act;
+  p.out_e4m3 = e.out_e4m3;
+  p.scale = e.scale;
+  p.err = dev_err();
+  switch (g.bn | (g.fp8 ? 1 : 0)) {
+    case 256: return launch_bn<256, false>(g, p, s);
+    case 257: return launch_bn<256, true>(g, p, s);
+    case 192: return launch_bn<192, false>(g, p, s);
+    case 193: return launch_bn<192, true>(g, p, s);
+    case 128: return launch_bn<128, false>(g, p, s);
+    case 129: return launch_bn<128, true>(g, p, s);
+    case 64: return launch_bn<64, false>(g, p, s);
+    case 65: return launch_bn<64, true>(g, p, s);
+    default: set_error("gemm: no kernel for tile width %d", g.bn); return SV_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace sv

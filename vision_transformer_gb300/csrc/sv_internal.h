@@ -1,0 +1,68 @@
+// Declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/sv.h"
+
+namespace sv {
+
+// ---- runtime state helpers (api.cu)
+void set_error(const char* fmt, ...);
+sv_status cuda_fail(cudaError_t e, const char* what);
+sv_status ensure_runtime();  // device error word, SM count
+int* dev_err();
+int num_sms();
+
+enum KernelKind { kKindGemm = 0, kKindAttn = 1, kKindLN = 2, kKindMapAttn = 3, kKindOther = 4, kNumKinds = 5 };
+
+// ---- tensor maps (gemm_tc.cu)
+sv_status make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw);
+
+// ---- GEMM: C = epilogue(A[M,K] . W[N,K]^T)
+struct GemmEpi {
+  const __half* bias = nullptr;      // [N]
+  const __half* pos = nullptr;       // [pos_rows, N], added by row m % pos_rows
+  int pos_rows = 1;
+  const __half* residual = nullptr;  // [M, N]
+  void* out = nullptr;               // [M, N] f16 or e4m3
+  int act = SV_ACT_NONE;
+  int out_e4m3 = 0;
+  float scale = 1.0f;
+};
+
+// The operand side of a GEMM: tensor maps for A and W plus the sizes.
+struct GemmOperands {
+  CUtensorMap ta, tw;
+  int M = 0, N = 0, K = 0;
+  int fp8 = 0;
+  int bn = 0;
+};
+
+// Tensor map of a K-major operand [rows, K] (row stride = K elements) with the
+// 128-byte swizzle the GEMM expects, box [box_rows, 128 bytes].
+sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int fp8, int box_rows);
+int gemm_pick_bn(int M, int N, int K);
+sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8);
+sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s);
+
+// ---- attention (attention.cu)
+// qkv: [B, T, 3*H*72] f16; o: [B, T, H*72] f16 / e4m3.
+sv_status attention_map(CUtensorMap* m, const void* qkv, int B, int T, int H);
+sv_status attention_launch(const CUtensorMap& m, void* o, int B, int T, int H, float scale, int out_e4m3,
+                           cudaStream_t s);
+
+// ---- elementwise (elementwise.cu)
+sv_status layernorm_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width,
+                           float eps, int out_e4m3, cudaStream_t s);
+sv_status pad_pixels_launch(const __half* pix, void* out, long rows, int P, int Kp, int out_e4m3, cudaStream_t s);
+sv_status quantize_launch(const __half* x, uint8_t* y, size_t n, cudaStream_t s);
+sv_status wait_probe_launch(unsigned int limit_us, cudaStream_t s);
+sv_status map_attn_launch(const __half* q, const __half* kv, void* out, int B, int T, int H, float scale,
+                          int out_e4m3, cudaStream_t s);
+
+}  // namespace sv
