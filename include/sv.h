@@ -163,6 +163,25 @@ sv_status sv_attention(const void* qkv, void* o, int batch, int heads, int token
  */
 sv_status sv_map_pool(const void* x, void* out, int batch, int gemm_dtype, void* stream);
 
+/*
+ * sv_map_pool without any device allocation by the library. The pages have no
+ * counterpart: this entry point exists for callers that cannot let a library
+ * call cudaMalloc at run time, e.g. a framework whose caching allocator or
+ * pre-sized pool owns the device memory, or a service with a fixed memory
+ * budget. Same arguments, computation and results as sv_map_pool (it uses the
+ * resident weights of sv_init_weights, which the caller sets up beforehand);
+ * images are pooled one at a time, so it is slower for large batches.
+ * Its scratch is one static device array of 8 MiB compiled into the library,
+ * held by every GPU that loads the library until the process exits. With the
+ * So400m/14 sizes that admits 1..256 images per call; larger batches (or
+ * models whose scratch would not fit) are rejected with SV_ERR_INVALID_ARG.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture. All calls share the array: calls whose GPU work overlaps
+ * (other streams or threads) race and must be serialised by the caller.
+ */
+sv_status sv_map_pool_static(const void* x, void* out, int batch, int gemm_dtype, void* stream);
+
 /* y[i] = e4m3 code of 16 * x[i] (saturating, round to nearest even); x f16, n % 16 == 0. */
 sv_status sv_quantize_e4m3(const void* x, void* y, size_t n, void* stream);
 

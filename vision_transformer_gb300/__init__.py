@@ -36,6 +36,7 @@ SIGNATURES = [
     ("sv_layernorm", _I, [_VP, _VP, _VP, _VP, _I, _I, _F, _I, _VP]),
     ("sv_attention", _I, [_VP, _VP, _I, _I, _I, _I, _F, _I, _VP]),
     ("sv_map_pool", _I, [_VP, _VP, _I, _I, _VP]),
+    ("sv_map_pool_static", _I, [_VP, _VP, _I, _I, _VP]),
     ("sv_quantize_e4m3", _I, [_VP, _VP, _SZ, _VP]),
     ("sv_make_pixels", _I, [_U64, _I, _VP, _VP]),
     ("sv_sync", _I, [_VP]),
@@ -135,6 +136,10 @@ def sv_attention(qkv, o, batch: int, heads: int, tokens: int, head_dim: int = 72
 
 def sv_map_pool(x, out, batch: int, gemm_dtype: int = SV_GEMM_F16, stream=None):
     _check("sv_map_pool", load().sv_map_pool(_ptr(x), _ptr(out), batch, gemm_dtype, _stream(stream)))
+
+
+def sv_map_pool_static(x, out, batch: int, gemm_dtype: int = SV_GEMM_F16, stream=None):
+    _check("sv_map_pool_static", load().sv_map_pool_static(_ptr(x), _ptr(out), batch, gemm_dtype, _stream(stream)))
 
 
 def sv_quantize_e4m3(x, y, n: int, stream=None):

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsv.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "attention.cu", "elementwise.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "attention.cu", "elementwise.cu", "map_static.cu"]
 HEADERS = ["ptx.cuh", "sv_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -521,6 +521,35 @@ sv_status ensure_runtime() {
   return SV_OK;
 }
 
+sv_status map_weights_view(MapWeightsView* v) {
+  SV_TRY(check_ready());
+  const Dims& d = g_w.d;
+  v->T = d.T;
+  v->D = d.D;
+  v->H = d.H;
+  v->F = d.F;
+  v->probe = g_w.probe;
+  v->q_w = g_w.mq_w;
+  v->q_b = g_w.mq_b;
+  v->kv_w = g_w.mkv_w;
+  v->kv_b = g_w.mkv_b;
+  v->out_w = g_w.mo_w;
+  v->out_b = g_w.mo_b;
+  v->ln_g = g_w.mln_g;
+  v->ln_b = g_w.mln_b;
+  v->fc1_w = g_w.mfc1_w;
+  v->fc1_b = g_w.mfc1_b;
+  v->fc2_w = g_w.mfc2_w;
+  v->fc2_b = g_w.mfc2_b;
+  v->probe8 = g_w.probe8;
+  v->q_w8 = g_w.mq_w8;
+  v->kv_w8 = g_w.mkv_w8;
+  v->out_w8 = g_w.mo_w8;
+  v->fc1_w8 = g_w.mfc1_w8;
+  v->fc2_w8 = g_w.mfc2_w8;
+  return SV_OK;
+}
+
 int* dev_err() { return g_rt.dev_err; }
 int num_sms() { return g_rt.sms; }
 

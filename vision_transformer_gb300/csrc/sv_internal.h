@@ -19,6 +19,14 @@ int num_sms();
 
 enum KernelKind { kKindGemm = 0, kKindAttn = 1, kKindLN = 2, kKindMapAttn = 3, kKindOther = 4, kNumKinds = 5 };
 
+// Read-only view of the resident MAP-head weights and model sizes (api.cu).
+struct MapWeightsView {
+  int T, D, H, F;
+  const __half *probe, *q_w, *q_b, *kv_w, *kv_b, *out_w, *out_b, *ln_g, *ln_b, *fc1_w, *fc1_b, *fc2_w, *fc2_b;
+  const uint8_t *probe8, *q_w8, *kv_w8, *out_w8, *fc1_w8, *fc2_w8;
+};
+sv_status map_weights_view(MapWeightsView* v);
+
 // ---- tensor maps (gemm_tc.cu)
 sv_status make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
                     const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw);
