@@ -92,9 +92,16 @@ struct Weights {
 };
 Weights g_w;
 
+// One GEMM of the path: operand and epilogue tensor maps, epilogue, logical K.
+struct GemmCall {
+  GemmOperands g;
+  GemmEpi e;
+  int k = 0;
+};
+
 // Buffers and operand maps of the MAP head for one batch size and dtype.
 struct MapPlan {
-  GemmOperands q, kv, out, fc1, fc2;
+  GemmCall q, kv, out, fc1, fc2;
   __half* qv = nullptr;  // [D] projected probe
   __half* KV = nullptr;  // [B*T, 2D]
   void* a = nullptr;     // [B, D] pooled attention (f16 / e4m3)
@@ -114,8 +121,8 @@ struct Plan {
   __half* QKV = nullptr;  // [M, 3D]
   void* O = nullptr;      // [M, D] attention output (GEMM operand)
   void* Hh = nullptr;     // [M, F] GELU output (GEMM operand)
-  GemmOperands patch;
-  std::vector<GemmOperands> qkv, out, fc1, fc2;
+  GemmCall patch;
+  std::vector<GemmCall> qkv, out, fc1, fc2;
   CUtensorMap attn;
   MapPlan map;
 };
@@ -269,7 +276,28 @@ struct Carver {
   }
 };
 
+sv_status make_call(GemmCall* c, const void* A, const void* W, int M, int N, int K, int fp8, const GemmEpi& e,
+                    int k_logical) {
+  c->e = e;
+  c->k = k_logical;
+  SV_TRY(gemm_prepare(&c->g, A, W, M, N, K, fp8));
+  return gemm_bind_epilogue(&c->g, c->e);
+}
+
+GemmEpi epi(const __half* bias, void* out, float scale, int act = SV_ACT_NONE, int out_e4m3 = 0,
+            const __half* residual = nullptr) {
+  GemmEpi e;
+  e.bias = bias;
+  e.out = out;
+  e.scale = scale;
+  e.act = act;
+  e.out_e4m3 = out_e4m3;
+  e.residual = residual;
+  return e;
+}
+
 // Buffers of the MAP head (carved from `c`); xf is the encoder-output operand.
+// The final projection's output is the caller's buffer: it is bound per call.
 sv_status build_map(MapPlan& m, Carver& c, const void* xf, int B, int fp8, bool carve_kv, __half* kv_alias) {
   const Dims& d = g_w.d;
   const size_t eb = fp8 ? 1 : 2;
@@ -280,13 +308,18 @@ sv_status build_map(MapPlan& m, Carver& c, const void* xf, int B, int fp8, bool 
   m.Ya = c.take(size_t(B) * d.D * eb);
   m.Ha = c.take(size_t(B) * d.F * eb);
   if (!c.base) return SV_OK;
-  SV_TRY(gemm_prepare(&m.q, fp8 ? (const void*)g_w.probe8 : g_w.probe, fp8 ? (const void*)g_w.mq_w8 : g_w.mq_w, 1,
-                      d.D, d.D, fp8));
-  SV_TRY(gemm_prepare(&m.kv, xf, fp8 ? (const void*)g_w.mkv_w8 : g_w.mkv_w, B * d.T, 2 * d.D, d.D, fp8));
-  SV_TRY(gemm_prepare(&m.out, m.a, fp8 ? (const void*)g_w.mo_w8 : g_w.mo_w, B, d.D, d.D, fp8));
-  SV_TRY(gemm_prepare(&m.fc1, m.Ya, fp8 ? (const void*)g_w.mfc1_w8 : g_w.mfc1_w, B, d.F, d.D, fp8));
-  SV_TRY(gemm_prepare(&m.fc2, m.Ha, fp8 ? (const void*)g_w.mfc2_w8 : g_w.mfc2_w, B, d.D, d.F, fp8));
-  return SV_OK;
+  const float sc = fp8 ? 1.0f / 256.0f : 1.0f;
+  const int D = d.D, F = d.F;
+  SV_TRY(make_call(&m.q, fp8 ? (const void*)g_w.probe8 : g_w.probe, fp8 ? (const void*)g_w.mq_w8 : g_w.mq_w, 1, D, D,
+                   fp8, epi(g_w.mq_b, m.qv, sc), D));
+  SV_TRY(make_call(&m.kv, xf, fp8 ? (const void*)g_w.mkv_w8 : g_w.mkv_w, B * d.T, 2 * D, D, fp8,
+                   epi(g_w.mkv_b, m.KV, sc), D));
+  SV_TRY(make_call(&m.out, m.a, fp8 ? (const void*)g_w.mo_w8 : g_w.mo_w, B, D, D, fp8, epi(g_w.mo_b, m.A, sc), D));
+  SV_TRY(make_call(&m.fc1, m.Ya, fp8 ? (const void*)g_w.mfc1_w8 : g_w.mfc1_w, B, F, D, fp8,
+                   epi(g_w.mfc1_b, m.Ha, sc, SV_ACT_GELU_TANH, fp8), D));
+  m.fc2.e = epi(g_w.mfc2_b, nullptr, sc, SV_ACT_NONE, 0, m.A);
+  m.fc2.k = F;
+  return gemm_prepare(&m.fc2.g, m.Ha, fp8 ? (const void*)g_w.mfc2_w8 : g_w.mfc2_w, B, D, F, fp8);
 }
 
 sv_status alloc_carved(Carver& c, void** mem, size_t* bytes) {
@@ -331,12 +364,16 @@ sv_status get_plan(int B, int fp8, Plan** out) {
     }
   }
   const int Mi = int(M);
+  const float sc = fp8 ? 1.0f / 256.0f : 1.0f;
   sv_status st = SV_OK;
   auto fail = [&](sv_status s) {
     cudaFree(p->mem);
     return s;
   };
-  if ((st = gemm_prepare(&p->patch, p->A0, fp8 ? (const void*)g_w.patch_w8 : g_w.patch_w, Mi, d.D, d.Kp, fp8)))
+  GemmEpi pe = epi(g_w.patch_b, p->X, sc);
+  pe.pos = g_w.pos;
+  pe.pos_rows = d.T;
+  if ((st = make_call(&p->patch, p->A0, fp8 ? (const void*)g_w.patch_w8 : g_w.patch_w, Mi, d.D, d.Kp, fp8, pe, d.P)))
     return fail(st);
   p->qkv.resize(size_t(d.L));
   p->out.resize(size_t(d.L));
@@ -344,10 +381,15 @@ sv_status get_plan(int B, int fp8, Plan** out) {
   p->fc2.resize(size_t(d.L));
   for (int l = 0; l < d.L; ++l) {
     const LayerW& w = g_w.layers[size_t(l)];
-    if ((st = gemm_prepare(&p->qkv[size_t(l)], p->Y, fp8 ? (const void*)w.qkv_w8 : w.qkv_w, Mi, 3 * d.D, d.D, fp8)) ||
-        (st = gemm_prepare(&p->out[size_t(l)], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8)) ||
-        (st = gemm_prepare(&p->fc1[size_t(l)], p->Y, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8)) ||
-        (st = gemm_prepare(&p->fc2[size_t(l)], p->Hh, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, Mi, d.D, d.F, fp8)))
+    const size_t i = size_t(l);
+    if ((st = make_call(&p->qkv[i], p->Y, fp8 ? (const void*)w.qkv_w8 : w.qkv_w, Mi, 3 * d.D, d.D, fp8,
+                        epi(w.qkv_b, p->QKV, sc), d.D)) ||
+        (st = make_call(&p->out[i], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8,
+                        epi(w.out_b, p->X, sc, SV_ACT_NONE, 0, p->X), d.D)) ||
+        (st = make_call(&p->fc1[i], p->Y, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8,
+                        epi(w.fc1_b, p->Hh, sc, SV_ACT_GELU_TANH, fp8), d.D)) ||
+        (st = make_call(&p->fc2[i], p->Hh, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, Mi, d.D, d.F, fp8,
+                        epi(w.fc2_b, p->X, sc, SV_ACT_NONE, 0, p->X), d.F)))
       return fail(st);
   }
   if ((st = attention_map(&p->attn, p->QKV, B, d.T, d.H))) return fail(st);
@@ -365,9 +407,9 @@ double gemm_bytes(const GemmOperands& g, const GemmEpi& e, int k_logical) {
   return b;
 }
 
-sv_status run_gemm(const GemmOperands& g, const GemmEpi& e, int k_logical, cudaStream_t s) {
-  Launch L(kKindGemm, gemm_flops(g, k_logical), gemm_bytes(g, e, k_logical), s);
-  return gemm_launch(g, e, s);
+sv_status run_gemm(const GemmCall& c, cudaStream_t s) {
+  Launch L(kKindGemm, gemm_flops(c.g, c.k), gemm_bytes(c.g, c.e, c.k), s);
+  return gemm_launch(c.g, c.e, s);
 }
 
 sv_status run_ln(const __half* x, const __half* gm, const __half* bt, void* y, int rows, int out_e4m3,
@@ -379,88 +421,48 @@ sv_status run_ln(const __half* x, const __half* gm, const __half* bt, void* y, i
 
 sv_status run_map(MapPlan& m, int B, int fp8, __half* out, cudaStream_t s) {
   const Dims& d = g_w.d;
-  const float sc = fp8 ? 1.0f / 256.0f : 1.0f;
-  GemmEpi e;
-  e.scale = sc;
-  e.bias = g_w.mq_b;
-  e.out = m.qv;
-  SV_TRY(run_gemm(m.q, e, d.D, s));
-  e.bias = g_w.mkv_b;
-  e.out = m.KV;
-  SV_TRY(run_gemm(m.kv, e, d.D, s));
+  SV_TRY(run_gemm(m.q, s));
+  SV_TRY(run_gemm(m.kv, s));
   {
     Launch L(kKindMapAttn, 4.0 * B * d.T * double(d.D), double(B) * d.T * 2 * d.D * 2.0, s);
     SV_TRY(map_attn_launch(m.qv, m.KV, m.a, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, s));
   }
-  e.bias = g_w.mo_b;
-  e.out = m.A;
-  SV_TRY(run_gemm(m.out, e, d.D, s));
+  SV_TRY(run_gemm(m.out, s));
   {
     Launch L(kKindLN, 8.0 * B * d.D, double(B) * d.D * 3.0, s);
     SV_TRY(layernorm_launch(m.A, g_w.mln_g, g_w.mln_b, m.Ya, B, d.D, 1e-6f, fp8, s));
   }
-  e.bias = g_w.mfc1_b;
-  e.act = SV_ACT_GELU_TANH;
-  e.out_e4m3 = fp8;
-  e.out = m.Ha;
-  SV_TRY(run_gemm(m.fc1, e, d.D, s));
-  e.bias = g_w.mfc2_b;
-  e.act = SV_ACT_NONE;
-  e.out_e4m3 = 0;
-  e.residual = m.A;
-  e.out = out;
-  return run_gemm(m.fc2, e, d.F, s);
+  SV_TRY(run_gemm(m.fc1, s));
+  if (m.fc2.e.out != out) {  // the caller's output buffer: rebind the final projection's output map
+    m.fc2.e.out = out;
+    SV_TRY(gemm_bind_epilogue(&m.fc2.g, m.fc2.e));
+  }
+  return run_gemm(m.fc2, s);
 }
 
 sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStream_t s) {
   const Dims& d = g_w.d;
   const int B = p.B, fp8 = p.fp8;
   const int M = B * d.T;
-  const float sc = fp8 ? 1.0f / 256.0f : 1.0f;
   {
     Launch L(kKindOther, 0.0, double(M) * (d.P * 2.0 + d.Kp * (fp8 ? 1.0 : 2.0)), s);
     SV_TRY(pad_pixels_launch(pixels, p.A0, M, d.P, d.Kp, fp8, s));
   }
-  GemmEpi e;
-  e.scale = sc;
-  e.bias = g_w.patch_b;
-  e.pos = g_w.pos;
-  e.pos_rows = d.T;
-  e.out = p.X;
-  SV_TRY(run_gemm(p.patch, e, d.P, s));
+  SV_TRY(run_gemm(p.patch, s));
   for (int l = 0; l < layers; ++l) {
     const LayerW& w = g_w.layers[size_t(l)];
+    const size_t i = size_t(l);
     SV_TRY(run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
-    GemmEpi q;
-    q.scale = sc;
-    q.bias = w.qkv_b;
-    q.out = p.QKV;
-    SV_TRY(run_gemm(p.qkv[size_t(l)], q, d.D, s));
+    SV_TRY(run_gemm(p.qkv[i], s));
     {
       Launch L(kKindAttn, 4.0 * B * d.H * double(d.T) * double(d.T) * 72.0,
                double(M) * 3 * d.D * 2.0 + double(M) * d.D * (fp8 ? 1.0 : 2.0), s);
       SV_TRY(attention_launch(p.attn, p.O, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, s));
     }
-    GemmEpi o;
-    o.scale = sc;
-    o.bias = w.out_b;
-    o.residual = p.X;
-    o.out = p.X;
-    SV_TRY(run_gemm(p.out[size_t(l)], o, d.D, s));
+    SV_TRY(run_gemm(p.out[i], s));
     SV_TRY(run_ln(p.X, w.ln2_g, w.ln2_b, p.Y, M, fp8, s));
-    GemmEpi f1;
-    f1.scale = sc;
-    f1.bias = w.fc1_b;
-    f1.act = SV_ACT_GELU_TANH;
-    f1.out_e4m3 = fp8;
-    f1.out = p.Hh;
-    SV_TRY(run_gemm(p.fc1[size_t(l)], f1, d.D, s));
-    GemmEpi f2;
-    f2.scale = sc;
-    f2.bias = w.fc2_b;
-    f2.residual = p.X;
-    f2.out = p.X;
-    SV_TRY(run_gemm(p.fc2[size_t(l)], f2, d.F, s));
+    SV_TRY(run_gemm(p.fc1[i], s));
+    SV_TRY(run_gemm(p.fc2[i], s));
   }
   SV_TRY(run_ln(p.X, g_w.enc_ln_g, g_w.enc_ln_b, p.Y, M, fp8, s));
   return run_map(p.map, B, fp8, out, s);
@@ -630,18 +632,12 @@ sv_status sv_gemm_bias_act(const void* A, const void* W, const void* bias, const
     return SV_ERR_INVALID_ARG;
   }
   SV_TRY(ensure_runtime());
-  GemmOperands g;
-  SV_TRY(gemm_prepare(&g, A, W, M, N, K, in_dtype));
-  GemmEpi e;
-  e.bias = static_cast<const __half*>(bias);
+  GemmEpi e = epi(static_cast<const __half*>(bias), C, scale, act, out_dtype, static_cast<const __half*>(residual));
   e.pos = static_cast<const __half*>(pos);
   e.pos_rows = pos_rows;
-  e.residual = static_cast<const __half*>(residual);
-  e.out = C;
-  e.act = act;
-  e.out_e4m3 = out_dtype;
-  e.scale = scale;
-  return run_gemm(g, e, K, static_cast<cudaStream_t>(stream));
+  GemmCall c;
+  SV_TRY(make_call(&c, A, W, M, N, K, in_dtype, e, K));
+  return run_gemm(c, static_cast<cudaStream_t>(stream));
 }
 
 sv_status sv_layernorm(const void* x, const void* gamma, const void* beta, void* y, int rows, int width, float eps,
@@ -717,7 +713,8 @@ sv_status sv_map_pool(const void* x, void* out, int batch, int gemm_dtype, void*
   } else {
     p = it->second.get();
     if (!fp8 && p->Y != x) {  // the KV operand map follows the caller's buffer
-      SV_TRY(gemm_prepare(&p->map.kv, x, g_w.mkv_w, batch * d.T, 2 * d.D, d.D, 0));
+      SV_TRY(gemm_prepare(&p->map.kv.g, x, g_w.mkv_w, batch * d.T, 2 * d.D, d.D, 0));
+      SV_TRY(gemm_bind_epilogue(&p->map.kv.g, p->map.kv.e));
       p->Y = const_cast<void*>(x);
     }
   }

@@ -15,7 +15,9 @@
 //               buffered so the epilogue of one tile overlaps the next tile's
 //               main loop;
 //   warps 2..5  epilogue: tcgen05.ld of 32 columns at a time, fused math,
-//               16-byte global stores.
+//               the 32 x 32 result block staged in swizzled shared memory and
+//               written by a TMA store; residual blocks arrive by TMA one
+//               chunk ahead.
 // F16 operands use kind::f16 (K = 16 per instruction); E4M3 operands use
 // kind::f8f6f4 (K = 32 per instruction) with the dequantisation scale
 // applied to the accumulator. All waits are bounded (ptx.cuh).
@@ -38,10 +40,13 @@ struct Cfg {
   static constexpr int kStageA = kBM * kBKBytes;
   static constexpr int kStageB = BN * kBKBytes;
   static constexpr int kStage = kStageA + kStageB;
-  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 192 ? 5 : (BN >= 128 ? 6 : 8));
+  static constexpr int kStages = BN >= 192 ? 4 : (BN >= 128 ? 6 : 8);
   static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
+  // epilogue staging: per epilogue warp two 32 x 32 output blocks and two residual blocks
+  static constexpr int kEpiBlock = 2048;
+  static constexpr int kEpiBytes = 4 * 2 * kEpiBlock * 2;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes;
+  static constexpr int kSmem = 1024 + kStages * kStage + kEpiBytes + kBarBytes;
   static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
@@ -52,8 +57,7 @@ struct Params {
   const __half* bias;
   const __half* pos;
   int pos_rows;
-  const __half* residual;
-  void* out;
+  int has_res;
   int act, out_e4m3;
   float scale;
   int* err;
@@ -76,83 +80,34 @@ __device__ __forceinline__ void load8h(const __half* p, float* f) {
   }
 }
 
-// Epilogue for 32 consecutive columns [n, n+32) of one row (n < N, N % 16 == 0).
-__device__ __forceinline__ void epilogue32(const Params& p, int row, int n, const uint32_t (&r)[32]) {
-  float v[32];
+__device__ __forceinline__ void add8h(const uint4& v, float* f) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * p.scale;
-  const int ngroups = min(4, (p.N - n) / 8);  // valid groups of 8 columns
-  const size_t rowoff = size_t(row) * size_t(p.N) + size_t(n);
-  if (p.bias) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      if (g < ngroups) {
-        float b[8];
-        load8h(p.bias + n + 8 * g, b);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[8 * g + i] += b[i];
-      }
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(h[i]);
+    f[2 * i] += t.x;
+    f[2 * i + 1] += t.y;
   }
-  if (p.pos) {
-    const size_t poff = size_t(row % p.pos_rows) * size_t(p.N) + size_t(n);
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      if (g < ngroups) {
-        float b[8];
-        load8h(p.pos + poff + 8 * g, b);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[8 * g + i] += b[i];
-      }
-  }
-  if (p.act == SV_ACT_GELU_TANH) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
-  }
-  if (p.residual) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      if (g < ngroups) {
-        float b[8];
-        load8h(p.residual + rowoff + 8 * g, b);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[8 * g + i] += b[i];
-      }
-  }
-  if (!p.out_e4m3) {
-    __half* o = static_cast<__half*>(p.out) + rowoff;
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      if (g < ngroups) {
-        uint4 w;
-        __half2* h = reinterpret_cast<__half2*>(&w);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[8 * g + 2 * i], v[8 * g + 2 * i + 1]);
-        *reinterpret_cast<uint4*>(o + 8 * g) = w;
-      }
-  } else {
-    uint8_t* o = static_cast<uint8_t*>(p.out) + rowoff;
-#pragma unroll
-    for (int g = 0; g < 2; ++g)
-      if (2 * g < ngroups) {  // N % 16 == 0: groups of 16 bytes are whole
-        uint4 w;
-        __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&w);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          q[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * v[16 * g + 2 * i], 16.0f * v[16 * g + 2 * i + 1]),
-                                          __NV_SATFINITE, __NV_E4M3);
-        *reinterpret_cast<uint4*>(o + 16 * g) = w;
-      }
-  }
+}
+
+// Number of 32-column chunks of tile column block nt that hold columns < N.
+__device__ __forceinline__ int tile_chunks(const Params& p, int nt, int bn) {
+  const int rem = p.N - nt * bn;
+  const int c = (rem + 31) / 32;
+  return c < bn / 32 ? c : bn / 32;
 }
 
 template <int BN, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const Params p) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
+                   const Params p) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5);
+  uint8_t* epi = smem + C::kStages * C::kStage;  // [4 warps][2] out blocks, then [4 warps][2] residual blocks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::kEpiBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_tfull = bar_empty + 8 * C::kStages;
   const uint32_t bar_tempty = bar_tfull + 16;
   const uint32_t bar_drain = bar_tempty + 16;
+  const uint32_t bar_res = bar_drain + 8;  // [4 warps][2]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -172,12 +128,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_tempty + 8 * a, 128);  // every epilogue thread arrives
     }
     mbar_init(bar_drain, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(bar_res + 8 * i, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmW);
+    prefetch_tmap(&tmC);
+    if (p.has_res) prefetch_tmap(&tmR);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -265,29 +224,144 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(bar_drain, 0, p.err);
     }
   } else {
-    const int sub = warp & 3;  // TMEM lanes 32*sub .. 32*sub+31
+    // Epilogue: warp ew owns TMEM lanes 32*sub .. +31, i.e. rows row0 .. row0+31 of
+    // each tile; each 32-column chunk is staged as a 32 x 32 block in shared memory
+    // (64-byte rows with the 64-byte swizzle for F16, 32-byte rows with the 32-byte
+    // swizzle for E4M3) and written by one TMA store, which also clips the M / N tails.
+    const int sub = warp & 3, ew = warp - 2;
+    uint8_t* obuf = epi + ew * 2 * C::kEpiBlock;
+    uint8_t* rbuf = epi + 4 * 2 * C::kEpiBlock + ew * 2 * C::kEpiBlock;
+    const uint32_t rbar = bar_res + 16 * ew;
+    // Residual loads in flight per buffer, with the phase parity that completes them.
+    bool res_issued[2] = {false, false};
+    uint32_t res_par[2] = {0, 0};
+    // Issues the residual load of chunk c of `tile` (the chunk with counter qq) into buffer qq & 1.
+    auto prefetch = [&](int tile, int c, int qq) {
+      const int b = qq & 1;
+      res_issued[b] = true;
+      res_par[b] = (qq >> 1) & 1;
+      if (lane == 0) {
+        const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(rbar + 8 * b, C::kEpiBlock);
+        tma_load_2d(smem_u32(rbuf + b * C::kEpiBlock), &tmR, rbar + 8 * b, nt * BN + 32 * c, mt * kBM + sub * 32);
+      }
+    };
+    if (p.has_res && int(blockIdx.x) < num_tiles) prefetch(blockIdx.x, 0, 0);
+    int q = 0;  // chunk counter of this warp: selects buffers and parities
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
       const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.err)) break;
+      // every lane waits; the outcome is made warp-uniform so warp-collective steps stay converged
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.err))) break;
       tc_fence_after();
-      const int row = mt * kBM + sub * 32 + lane;
+      const int row0 = mt * kBM + sub * 32;
+      const int row = row0 + lane;
       const int n0 = nt * BN;
+      const int nch = tile_chunks(p, nt, BN);
       const uint32_t tbase = tmem_base + uint32_t(acc * BN) + (uint32_t(sub * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < nch; ++c, ++q) {
+        const int b = q & 1;
+        if (p.has_res) {  // the next chunk's residual goes into the other buffer
+          int t2 = tile, c2 = c + 1;
+          if (c2 >= nch) {
+            t2 = tile + gridDim.x;
+            c2 = 0;
+          }
+          if (t2 < num_tiles) prefetch(t2, c2, q + 1);
+        }
         const int n = n0 + 32 * c;
-        if (n >= p.N) break;  // warp-uniform
         uint32_t r[32];
         tmem_ld32(tbase + 32 * c, r);
         tmem_ld_wait();
-        if (row < p.M) epilogue32(p, row, n, r);
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * p.scale;
+        const int ngroups = min(4, (p.N - n) / 8);  // groups of 8 columns below N
+        if (p.bias) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if (g < ngroups) {
+              float bb[8];
+              load8h(p.bias + n + 8 * g, bb);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[8 * g + i] += bb[i];
+            }
+        }
+        if (p.pos) {
+          const size_t poff = size_t(row % p.pos_rows) * size_t(p.N) + size_t(n);
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if (g < ngroups) {
+              float bb[8];
+              load8h(p.pos + poff + 8 * g, bb);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[8 * g + i] += bb[i];
+            }
+        }
+        if (p.act == SV_ACT_GELU_TANH) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+        }
+        if (p.has_res) {
+          if (!__all_sync(0xffffffffu, mbar_wait(rbar + 8 * b, (q >> 1) & 1, abort_flag, p.err))) {
+            ok = false;
+            break;
+          }
+          const uint8_t* rrow = rbuf + b * C::kEpiBlock + lane * 64;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint4 u = *reinterpret_cast<const uint4*>(rrow + 16 * (g ^ ((lane >> 1) & 3)));
+            add8h(u, v + 8 * g);
+          }
+        }
+        // the store issued two chunks ago from this buffer has finished reading it
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        uint8_t* blk = obuf + b * C::kEpiBlock;
+        if (!p.out_e4m3) {
+          uint8_t* orow = blk + lane * 64;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint4 w;
+            __half2* h = reinterpret_cast<__half2*>(&w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[8 * g + 2 * i], v[8 * g + 2 * i + 1]);
+            *reinterpret_cast<uint4*>(orow + 16 * (g ^ ((lane >> 1) & 3))) = w;
+          }
+        } else {
+          uint8_t* orow = blk + lane * 32;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            uint4 w;
+            __nv_fp8x2_storage_t* qq = reinterpret_cast<__nv_fp8x2_storage_t*>(&w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              qq[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * v[16 * g + 2 * i], 16.0f * v[16 * g + 2 * i + 1]),
+                                               __NV_SATFINITE, __NV_E4M3);
+            *reinterpret_cast<uint4*>(orow + 16 * (g ^ ((lane >> 2) & 1))) = w;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, smem_u32(blk), n, row0);
+          bulk_commit();
+        }
       }
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * acc);
     }
+    if (lane == 0) {
+      bulk_wait_all();  // every store has read shared memory and written global memory
+      for (int b = 0; b < 2; ++b)
+        if (res_issued[b]) mbar_wait_bounded(rbar + 8 * b, res_par[b], p.err);
+    }
+    __syncwarp();
   }
   __syncthreads();
   if (warp == 1) {
@@ -308,7 +382,7 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
   }
   const int tiles = prm.m_tiles * prm.n_tiles;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kThreads, C::kSmem, s>>>(g.ta, g.tw, prm);
+  kern<<<grid, kThreads, C::kSmem, s>>>(g.ta, g.tw, g.tc, g.has_res ? g.tr : g.tc, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return SV_OK;
@@ -367,8 +441,11 @@ sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int
                    box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Output-tile width: estimated main-loop time = waves x per-tile time, where a
-// tile's K-step costs max(tensor time, shared-memory operand traffic / 128 B per clock).
+// Output-tile width: estimated main-loop time = waves x per-tile time. A tile's
+// K-step of 16 costs the larger of its tensor time (BN / 2 cycles at 8192
+// FLOP/clock/SM) and its operand traffic from L2, (128 + BN) x 32 bytes at
+// about 90 bytes/clock/SM (the L2 bandwidth measured under ncu: 16 TB/s at 61%
+// of its peak).
 int gemm_pick_bn(int M, int N, int K) {
   const int cand[4] = {256, 192, 128, 64};
   const int sms = num_sms() > 0 ? num_sms() : 148;
@@ -377,8 +454,8 @@ int gemm_pick_bn(int M, int N, int K) {
   const int mt = (M + kBM - 1) / kBM;
   for (int bn : cand) {
     const double mma = bn / 2.0;
-    const double smem = (kBM * 32.0 + bn * 32.0) / 128.0;
-    const double step = mma > smem ? mma : smem;
+    const double l2 = (kBM + bn) * 32.0 / 90.0;
+    const double step = mma > l2 ? mma : l2;
     const long tiles = long(mt) * ((N + bn - 1) / bn);
     const long waves = (tiles + sms - 1) / sms;
     const double t = double(waves) * step * double((K + 15) / 16);
@@ -401,7 +478,33 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
   return gemm_operand_map(&g->tw, W, N, K, fp8, g->bn);
 }
 
+// Output (and residual) maps of a [M, N] row-major matrix in 32 x 32 blocks:
+// F16 with 64-byte rows and the 64-byte swizzle, E4M3 with 32-byte rows and
+// the 32-byte swizzle (the layout the epilogue writes in shared memory).
+sv_status gemm_output_map(CUtensorMap* m, const void* ptr, int M, int N, int e4m3) {
+  const uint64_t dims[2] = {uint64_t(N), uint64_t(M)};
+  const uint64_t strides[1] = {uint64_t(N) * (e4m3 ? 1u : 2u)};
+  const uint32_t box[2] = {32, 32};
+  return make_tmap(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, dims, strides,
+                   box, e4m3 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e) {
+  sv_status st = gemm_output_map(&g->tc, e.out, g->M, g->N, e.out_e4m3);
+  if (st != SV_OK) return st;
+  g->has_res = e.residual != nullptr;
+  g->out = e.out;
+  g->out_e4m3 = e.out_e4m3;
+  g->res = e.residual;
+  if (g->has_res) return gemm_output_map(&g->tr, e.residual, g->M, g->N, 0);
+  return SV_OK;
+}
+
 sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
+  if (e.out != g.out || e.out_e4m3 != g.out_e4m3 || e.residual != g.res) {
+    set_error("gemm: epilogue buffers differ from the ones the tensor maps were built for");
+    return SV_ERR_INVALID_ARG;
+  }
   Params p;
   p.M = g.M;
   p.N = g.N;
@@ -413,8 +516,7 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.bias = e.bias;
   p.pos = e.pos;
   p.pos_rows = e.pos_rows > 0 ? e.pos_rows : 1;
-  p.residual = e.residual;
-  p.out = e.out;
+  p.has_res = e.residual != nullptr;
   p.act = e.act;
   p.out_e4m3 = e.out_e4m3;
   p.scale = e.scale;

@@ -136,6 +136,7 @@ extern "C" sv_status sv_map_pool_static(const void* x, void* out, int batch, int
                         fp8));
   e.bias = w.q_b;
   e.out = q;
+  SV_TRY_S(gemm_bind_epilogue(&g, e));
   SV_TRY_S(gemm_launch(g, e, st));
   // one image at a time: [K V] = x_b . Wkv + bkv, then the single-query attention into a[b]
   const size_t img = size_t(w.T) * w.D;
@@ -149,6 +150,7 @@ extern "C" sv_status sv_map_pool_static(const void* x, void* out, int batch, int
     SV_TRY_S(gemm_prepare(&g, A_op, fp8 ? (const void*)w.kv_w8 : w.kv_w, w.T, 2 * w.D, w.D, fp8));
     e.bias = w.kv_b;
     e.out = kv;
+    SV_TRY_S(gemm_bind_epilogue(&g, e));
     SV_TRY_S(gemm_launch(g, e, st));
     SV_TRY_S(map_attn_launch(q, kv, static_cast<char*>(a) + size_t(b) * w.D * eb, 1, w.T, w.H, attn_scale, fp8,
                              st));
@@ -157,6 +159,7 @@ extern "C" sv_status sv_map_pool_static(const void* x, void* out, int batch, int
   SV_TRY_S(gemm_prepare(&g, a, fp8 ? (const void*)w.out_w8 : w.out_w, batch, w.D, w.D, fp8));
   e.bias = w.out_b;
   e.out = A;
+  SV_TRY_S(gemm_bind_epilogue(&g, e));
   SV_TRY_S(gemm_launch(g, e, st));
   SV_TRY_S(layernorm_launch(A, w.ln_g, w.ln_b, Ya, batch, w.D, 1e-6f, fp8, st));
   SV_TRY_S(gemm_prepare(&g, Ya, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, batch, w.F, w.D, fp8));
@@ -164,6 +167,7 @@ extern "C" sv_status sv_map_pool_static(const void* x, void* out, int batch, int
   e.act = SV_ACT_GELU_TANH;
   e.out_e4m3 = fp8;
   e.out = Ha;
+  SV_TRY_S(gemm_bind_epilogue(&g, e));
   SV_TRY_S(gemm_launch(g, e, st));
   SV_TRY_S(gemm_prepare(&g, Ha, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, batch, w.D, w.F, fp8));
   e.bias = w.fc2_b;
@@ -171,5 +175,6 @@ extern "C" sv_status sv_map_pool_static(const void* x, void* out, int batch, int
   e.out_e4m3 = 0;
   e.residual = A;
   e.out = out;
+  SV_TRY_S(gemm_bind_epilogue(&g, e));
   return gemm_launch(g, e, st);
 }

@@ -45,10 +45,14 @@ struct GemmEpi {
 
 // The operand side of a GEMM: tensor maps for A and W plus the sizes.
 struct GemmOperands {
-  CUtensorMap ta, tw;
+  CUtensorMap ta, tw, tc, tr;  // A, W, output, residual
   int M = 0, N = 0, K = 0;
   int fp8 = 0;
   int bn = 0;
+  int has_res = 0;
+  const void* out = nullptr;  // epilogue buffers the output / residual maps describe
+  const void* res = nullptr;
+  int out_e4m3 = 0;
 };
 
 // Tensor map of a K-major operand [rows, K] (row stride = K elements) with the
@@ -56,6 +60,8 @@ struct GemmOperands {
 sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int fp8, int box_rows);
 int gemm_pick_bn(int M, int N, int K);
 sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8);
+// Builds the output / residual tensor maps for the epilogue's buffers (must precede gemm_launch).
+sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e);
 sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s);
 
 // ---- attention (attention.cu)
