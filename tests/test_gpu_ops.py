@@ -143,7 +143,7 @@ def _attn_ref(qkv, H):
 
 
 @pytest.mark.parametrize("B,H,T,sharp", [(1, 2, 4, 1.0), (2, 16, 729, 1.0), (1, 3, 200, 3.0), (8, 16, 729, 2.0),
-                                         (1, 1, 129, 1.0), (1, 2, 1, 1.0)])
+                                         (1, 1, 129, 1.0), (1, 2, 1, 1.0), (3, 4, 300, 1.5)])
 def test_attention(sv, B, H, T, sharp):
     D = H * 72
     qkv = synth.normal(80 + T, 1, (B, T, 3 * D))

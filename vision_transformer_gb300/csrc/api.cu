@@ -118,16 +118,17 @@ struct Plan {
   void* A0 = nullptr;     // [M, Kp] staged pixels
   __half* X = nullptr;    // [M, D] residual stream
   void* Y = nullptr;      // [M, D] LayerNorm output (GEMM operand)
-  __half* QKV = nullptr;  // [M, 3D]
+  __half* QKV = nullptr;  // head-blocked Q/K/V for attention; the MAP KV projection reuses it row-major
   void* O = nullptr;      // [M, D] attention output (GEMM operand)
   void* Hh = nullptr;     // [M, F] GELU output (GEMM operand)
   GemmCall patch;
   std::vector<GemmCall> qkv, out, fc1, fc2;
-  CUtensorMap attn;
   MapPlan map;
 };
 std::map<std::pair<int, int>, std::unique_ptr<Plan>> g_plans;      // sv_encode
 std::map<std::pair<int, int>, std::unique_ptr<Plan>> g_map_plans;  // sv_map_pool
+void* g_attn_scratch = nullptr;  // head-blocked copy of sv_attention's input
+size_t g_attn_scratch_bytes = 0;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -136,6 +137,9 @@ void free_plans() {
   for (auto& kv : g_map_plans) cudaFree(kv.second->mem);
   g_plans.clear();
   g_map_plans.clear();
+  if (g_attn_scratch) cudaFree(g_attn_scratch);
+  g_attn_scratch = nullptr;
+  g_attn_scratch_bytes = 0;
 }
 
 void free_weights() {
@@ -354,7 +358,8 @@ sv_status get_plan(int B, int fp8, Plan** out) {
     p->A0 = c.take(M * d.Kp * eb);
     p->X = static_cast<__half*>(c.take(M * d.D * 2));
     p->Y = c.take(M * d.D * eb);
-    p->QKV = static_cast<__half*>(c.take(M * 3 * d.D * 2));
+    const size_t qkv_bytes = attention_blocked_bytes(B, d.T, d.H);
+    p->QKV = static_cast<__half*>(c.take(qkv_bytes > M * 3 * d.D * 2 ? qkv_bytes : M * 3 * d.D * 2));
     p->O = c.take(M * d.D * eb);
     p->Hh = c.take(M * d.F * eb);
     SV_TRY(build_map(p->map, c, p->Y, B, fp8, false, p->QKV));
@@ -382,8 +387,12 @@ sv_status get_plan(int B, int fp8, Plan** out) {
   for (int l = 0; l < d.L; ++l) {
     const LayerW& w = g_w.layers[size_t(l)];
     const size_t i = size_t(l);
-    if ((st = make_call(&p->qkv[i], p->Y, fp8 ? (const void*)w.qkv_w8 : w.qkv_w, Mi, 3 * d.D, d.D, fp8,
-                        epi(w.qkv_b, p->QKV, sc), d.D)) ||
+    GemmEpi qe = epi(w.qkv_b, p->QKV, sc);
+    qe.blk_out = p->QKV;
+    qe.blk_T = d.T;
+    qe.blk_H = d.H;
+    qe.blk_B = B;
+    if ((st = make_call(&p->qkv[i], p->Y, fp8 ? (const void*)w.qkv_w8 : w.qkv_w, Mi, 3 * d.D, d.D, fp8, qe, d.D)) ||
         (st = make_call(&p->out[i], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8,
                         epi(w.out_b, p->X, sc, SV_ACT_NONE, 0, p->X), d.D)) ||
         (st = make_call(&p->fc1[i], p->Y, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8,
@@ -392,7 +401,6 @@ sv_status get_plan(int B, int fp8, Plan** out) {
                         epi(w.fc2_b, p->X, sc, SV_ACT_NONE, 0, p->X), d.F)))
       return fail(st);
   }
-  if ((st = attention_map(&p->attn, p->QKV, B, d.T, d.H))) return fail(st);
   *out = p.get();
   g_plans[key] = std::move(p);
   return SV_OK;
@@ -457,7 +465,7 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
     {
       Launch L(kKindAttn, 4.0 * B * d.H * double(d.T) * double(d.T) * 72.0,
                double(M) * 3 * d.D * 2.0 + double(M) * d.D * (fp8 ? 1.0 : 2.0), s);
-      SV_TRY(attention_launch(p.attn, p.O, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, s));
+      SV_TRY(attention_launch(p.QKV, p.O, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, s));
     }
     SV_TRY(run_gemm(p.out[i], s));
     SV_TRY(run_ln(p.X, w.ln2_g, w.ln2_b, p.Y, M, fp8, s));
@@ -674,11 +682,29 @@ sv_status sv_attention(const void* qkv, void* o, int batch, int heads, int token
     return SV_ERR_INVALID_ARG;
   }
   SV_TRY(ensure_runtime());
-  CUtensorMap m;
-  SV_TRY(attention_map(&m, qkv, batch, tokens, heads));
+  const size_t need = attention_blocked_bytes(batch, tokens, heads);
+  if (need > g_attn_scratch_bytes) {  // grows monotonically; freed by sv_shutdown
+    if (g_attn_scratch) {
+      SV_CHECK_CUDA(cudaDeviceSynchronize(), "sv_attention");
+      cudaFree(g_attn_scratch);
+      g_attn_scratch = nullptr;
+      g_attn_scratch_bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&g_attn_scratch, need);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      set_error("sv_attention: cudaMalloc of %zu bytes failed", need);
+      return SV_ERR_OOM;
+    }
+    g_attn_scratch_bytes = need;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    Launch L(kKindOther, 0.0, double(batch) * tokens * 3 * heads * 72 * 4.0, s);
+    SV_TRY(attention_repack_launch(static_cast<const __half*>(qkv), g_attn_scratch, batch, tokens, heads, s));
+  }
   Launch L(kKindAttn, 4.0 * batch * heads * double(tokens) * tokens * 72.0, 0.0, s);
-  return attention_launch(m, o, batch, tokens, heads, scale, out_dtype, s);
+  return attention_launch(g_attn_scratch, o, batch, tokens, heads, scale, out_dtype, s);
 }
 
 sv_status sv_map_pool(const void* x, void* out, int batch, int gemm_dtype, void* stream) {

@@ -13,7 +13,10 @@
 //   warp 1      allocates TMEM and issues tcgen05.mma (M = 128, N = BN) from
 //               one thread; the accumulator (F32) lives in TMEM, double
 //               buffered so the epilogue of one tile overlaps the next tile's
-//               main loop;
+//               main loop. With two or more row tiles the CTAs run in pairs
+//               (clusters of 2) that share one M = 256 MMA (cta_group::2):
+//               each CTA stages its 128 rows of A and half of the W tile, the
+//               leader issues the MMAs, each CTA's TMEM holds its 128 rows;
 //   warps 2..5  epilogue: tcgen05.ld of 32 columns at a time, fused math,
 //               the 32 x 32 result block staged in swizzled shared memory and
 //               written by a TMA store; residual blocks arrive by TMA one
@@ -34,18 +37,24 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBKBytes = 128;  // K bytes per stage: one 128-byte swizzle row
 constexpr int kThreads = 192;
+// Widest output tile used with CTA pairs (its TMEM: 2 x BN columns per CTA).
+constexpr int kPairMaxBn = 256;
 
-template <int BN>
+// PAIR: the two CTAs of a cluster share one 256-row MMA (cta_group::2): each
+// holds its 128 rows of A and half of the W tile per stage, and the tensor core
+// reads the other half from the peer.
+template <int BN, bool PAIR>
 struct Cfg {
   static constexpr int kStageA = kBM * kBKBytes;
-  static constexpr int kStageB = BN * kBKBytes;
+  static constexpr int kStageB = (PAIR ? BN / 2 : BN) * kBKBytes;
   static constexpr int kStage = kStageA + kStageB;
-  static constexpr int kStages = BN >= 192 ? 4 : (BN >= 128 ? 6 : 8);
-  static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
   // epilogue staging: per epilogue warp two 32 x 32 output blocks and two residual blocks
   static constexpr int kEpiBlock = 2048;
   static constexpr int kEpiBytes = 4 * 2 * kEpiBlock * 2;
   static constexpr int kBarBytes = 256;
+  static constexpr int kBudget = 232448 - 1024 - kEpiBytes - kBarBytes;
+  static constexpr int kStages = kBudget / kStage < 8 ? kBudget / kStage : 8;
+  static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
   static constexpr int kSmem = 1024 + kStages * kStage + kEpiBytes + kBarBytes;
   static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -61,12 +70,20 @@ struct Params {
   int act, out_e4m3;
   float scale;
   int* err;
+  // head-blocked output (fused QKV projection feeding attention), or null
+  uint8_t* blk;
+  int blk_T, blk_H, blk_B, blk_tiles;
 };
 
+// GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), with
+// the hardware tanh (one MUFU operation; relative error about 2^-11, the F16
+// output's own rounding).
 __device__ __forceinline__ float gelu_tanh(float x) {
-  // 0.5 x (1 + tanh(u)) == x / (1 + exp(-2u)),  u = sqrt(2/pi) (x + 0.044715 x^3)
   const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-  return __fdividef(x, 1.0f + __expf(-2.0f * u));
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(u));
+  const float hx = 0.5f * x;
+  return fmaf(hx, t, hx);
 }
 
 __device__ __forceinline__ void load8h(const __half* p, float* f) {
@@ -97,12 +114,21 @@ __device__ __forceinline__ int tile_chunks(const Params& p, int nt, int bn) {
   return c < bn / 32 ? c : bn / 32;
 }
 
-template <int BN, bool FP8>
+// Work item `it` -> output tile (mt, nt). With PAIR an item is a 256-row tile
+// of two vertically adjacent 128-row tiles; the CTA of cluster rank r takes
+// m-tile 2 * pair + r.
+template <bool PAIR>
+__device__ __forceinline__ void tile_of(const Params& p, int it, int rank, int& mt, int& nt) {
+  nt = it % p.n_tiles;
+  mt = PAIR ? 2 * (it / p.n_tiles) + rank : it / p.n_tiles;
+}
+
+template <int BN, bool FP8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                    const Params p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + C::kStages * C::kStage;  // [4 warps][2] out blocks, then [4 warps][2] residual blocks
@@ -118,14 +144,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_drain = bar_tempty + 16;
   const uint32_t bar_res = bar_drain + 8;  // [4 warps][2]
 
+  // Work items: tiles, or (PAIR) 256-row tiles shared by the two CTAs of a cluster.
+  const int rank = PAIR ? int(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int it0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
+  const int it_step = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
+  const int num_items = PAIR ? ((p.m_tiles + 1) / 2) * p.n_tiles : p.m_tiles * p.n_tiles;
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, 1);   // PAIR: the leader's producer arms it for both CTAs' bytes
+      mbar_init(bar_empty + 8 * s, 1);  // PAIR: released by the leader's MMA commit in both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
-      mbar_init(bar_tempty + 8 * a, 128);  // every epilogue thread arrives
+      mbar_init(bar_tempty + 8 * a, PAIR ? 256 : 128);  // every epilogue thread (of both CTAs) arrives
     }
     mbar_init(bar_drain, 1);
     for (int i = 0; i < 8; ++i) mbar_init(bar_res + 8 * i, 1);
@@ -139,14 +172,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.has_res) prefetch_tmap(&tmR);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_tiles = p.m_tiles * p.n_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -154,19 +192,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_phase = 0;  // stages with loads in flight, and their phase bit
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+      for (int it = it0; it < num_items && ok; it += it_step) {
+        int mt, nt;
+        tile_of<PAIR>(p, it, rank, mt, nt);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
           const uint32_t fb = bar_full + 8 * stage;
-          mbar_arrive_expect_tx(fb, C::kStage);
           const uint32_t sa = smem_u32(smem + stage * C::kStage);
           const int kc = kb * (FP8 ? 128 : 64);
-          tma_load_2d(sa, &tmA, fb, kc, mt * kBM);
-          tma_load_2d(sa + C::kStageA, &tmW, fb, kc, nt * BN);
+          if (PAIR) {  // both CTAs' copies complete on the leader's barrier
+            if (leader) mbar_arrive_expect_tx(fb, 2 * C::kStage);
+            const uint32_t fb_lead = mapa_shared(fb, 0);
+            tma_load_2d_pair(sa, &tmA, fb_lead, kc, mt * kBM);
+            tma_load_2d_pair(sa + C::kStageA, &tmW, fb_lead, kc, nt * BN + rank * (BN / 2));
+          } else {
+            mbar_arrive_expect_tx(fb, C::kStage);
+            tma_load_2d(sa, &tmA, fb, kc, mt * kBM);
+            tma_load_2d(sa + C::kStageA, &tmW, fb, kc, nt * BN);
+          }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) {
@@ -175,19 +221,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Every copy this thread issued lands before the CTA can exit (immediate
-      // on the normal path, where the MMA warp already consumed them all).
+      // Every copy this thread issued lands (and, under PAIR, every stage release of the
+      // leader's MMA lands in this CTA) before the CTA can exit; immediate on the normal path.
       for (int st = 0; st < C::kStages; ++st)
-        if (issued & (1u << st)) mbar_wait_bounded(bar_full + 8 * st, (issued_phase >> st) & 1, p.err);
+        if (issued & (1u << st)) {
+          if (PAIR)
+            mbar_wait_bounded(bar_empty + 8 * st, (issued_phase >> st) & 1, p.err);
+          else
+            mbar_wait_bounded(bar_full + 8 * st, (issued_phase >> st) & 1, p.err);
+        }
+      // After an abort under PAIR, copies issued toward stages nobody consumes may
+      // still be in flight: give them time to land (about 100 us) before leaving.
+      if (PAIR && *abort_flag) {
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {
+        }
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(kBM, BN, 0, false);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = make_idesc(PAIR ? 2 * kBM : kBM, BN, 0, false);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+      for (int it = it0; it < num_items && ok; it += it_step, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag, p.err)) break;
@@ -206,22 +264,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ad = make_sdesc(sa + 32 * j, 16, 1024, 2);
             const uint64_t bd = make_sdesc(sb + 32 * j, 16, 1024, 2);
             const uint32_t accum = (kb | j) != 0;
-            if (FP8)
-              mma_f8(d, ad, bd, idesc, accum);
-            else
-              mma_f16(d, ad, bd, idesc, accum);
+            if (PAIR) {
+              if (FP8)
+                mma_f8_pair(d, ad, bd, idesc, accum);
+              else
+                mma_f16_pair(d, ad, bd, idesc, accum);
+            } else {
+              if (FP8)
+                mma_f8(d, ad, bd, idesc, accum);
+              else
+                mma_f16(d, ad, bd, idesc, accum);
+            }
           }
-          tc_commit(bar_empty + 8 * stage);  // frees the stage when these MMAs finish
+          // frees the stage (in both CTAs under PAIR) when these MMAs finish
+          if (PAIR)
+            tc_commit_pair_mc(bar_empty + 8 * stage, uint16_t(3));
+          else
+            tc_commit(bar_empty + 8 * stage);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
-        if (ok) tc_commit(bar_tfull + 8 * acc);
+        if (ok) {
+          if (PAIR)
+            tc_commit_pair_mc(bar_tfull + 8 * acc, uint16_t(3));
+          else
+            tc_commit(bar_tfull + 8 * acc);
+        }
       }
       // All MMAs this thread issued complete before TMEM is released.
-      tc_commit(bar_drain);
+      if (PAIR)
+        tc_commit_pair_mc(bar_drain, uint16_t(1));
+      else
+        tc_commit(bar_drain);
       mbar_wait_bounded(bar_drain, 0, p.err);
+      // Under PAIR the epilogues of both CTAs release accumulators on this CTA's
+      // barriers: wait for the last releases so none lands after this CTA exits.
+      if (PAIR)
+        for (int a = 0; a < 2 && a < local; ++a) {
+          const int last = (local - 1 - a) >= 0 ? ((local - 1 - a) >> 1) : 0;  // use index of the last use of acc
+          const int acc = (local - 1 - a) & 1;
+          mbar_wait_bounded(bar_tempty + 8 * acc, uint32_t(last) & 1, p.err);
+        }
     }
   } else {
     // Epilogue: warp ew owns TMEM lanes 32*sub .. +31, i.e. rows row0 .. row0+31 of
@@ -236,23 +321,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool res_issued[2] = {false, false};
     uint32_t res_par[2] = {0, 0};
     // Issues the residual load of chunk c of `tile` (the chunk with counter qq) into buffer qq & 1.
-    auto prefetch = [&](int tile, int c, int qq) {
+    auto prefetch = [&](int mt, int nt, int c, int qq) {
       const int b = qq & 1;
       res_issued[b] = true;
       res_par[b] = (qq >> 1) & 1;
       if (lane == 0) {
-        const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(rbar + 8 * b, C::kEpiBlock);
         tma_load_2d(smem_u32(rbuf + b * C::kEpiBlock), &tmR, rbar + 8 * b, nt * BN + 32 * c, mt * kBM + sub * 32);
       }
     };
-    if (p.has_res && int(blockIdx.x) < num_tiles) prefetch(blockIdx.x, 0, 0);
+    // residual prefetch of chunk c of work item `it` (the chunk with counter qq)
+    auto prefetch_item = [&](int it, int c, int qq) {
+      int mt, nt;
+      tile_of<PAIR>(p, it, rank, mt, nt);
+      prefetch(mt, nt, c, qq);
+    };
+    if (p.has_res && it0 < num_items) prefetch_item(it0, 0, 0);
     int q = 0;  // chunk counter of this warp: selects buffers and parities
     int local = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
-      const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+    const uint32_t tempty_lead0 = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
+    for (int it = it0; it < num_items && ok; it += it_step, ++local) {
+      int mt, nt;
+      tile_of<PAIR>(p, it, rank, mt, nt);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       // every lane waits; the outcome is made warp-uniform so warp-collective steps stay converged
@@ -267,12 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < nch; ++c, ++q) {
         const int b = q & 1;
         if (p.has_res) {  // the next chunk's residual goes into the other buffer
-          int t2 = tile, c2 = c + 1;
+          int it2 = it, c2 = c + 1;
           if (c2 >= nch) {
-            t2 = tile + gridDim.x;
+            it2 = it + it_step;
             c2 = 0;
           }
-          if (t2 < num_tiles) prefetch(t2, c2, q + 1);
+          if (it2 < num_items) prefetch_item(it2, c2, q + 1);
         }
         const int n = n0 + 32 * c;
         uint32_t r[32];
@@ -319,6 +411,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             add8h(u, v + 8 * g);
           }
         }
+        if (p.blk) {  // head-blocked layout for attention: 16-byte stores, consecutive rows contiguous
+          if (row < p.M) {
+            const int D = p.blk_H * 72;
+            const int bimg = row / p.blk_T, t = row - bimg * p.blk_T;
+            const size_t rowoff = (size_t(bimg) * p.blk_H * p.blk_tiles + (t >> 7)) * 18432 + (t & 127) * 16;
+            const size_t which_stride = size_t(p.blk_B) * p.blk_H * p.blk_tiles * 18432;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              if (g < ngroups) {
+                const int col = n + 8 * g;
+                const int which = col >= 2 * D ? 2 : (col >= D ? 1 : 0);
+                const int rem = col - which * D;
+                const int h = (rem * 58255) >> 22;  // rem / 72, exact for rem < 4096
+                const int cg = (rem - h * 72) >> 3;
+                uint4 w;
+                __half2* hh = reinterpret_cast<__half2*>(&w);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) hh[i] = __floats2half2_rn(v[8 * g + 2 * i], v[8 * g + 2 * i + 1]);
+                *reinterpret_cast<uint4*>(p.blk + which * which_stride + rowoff +
+                                          size_t(h) * p.blk_tiles * 18432 + cg * 2048) = w;
+              }
+          }
+          continue;
+        }
         // the store issued two chunks ago from this buffer has finished reading it
         if (lane == 0) bulk_wait_read<1>();
         __syncwarp();
@@ -354,7 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(bar_tempty + 8 * acc);
+      if (PAIR)
+        mbar_arrive_cluster(tempty_lead0 + 8 * acc);  // the leader's MMA waits for both CTAs
+      else
+        mbar_arrive(bar_tempty + 8 * acc);
     }
     if (lane == 0) {
       bulk_wait_all();  // every store has read shared memory and written global memory
@@ -364,26 +483,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
   __syncthreads();
+  if (PAIR) cluster_sync();  // the leader's MMAs write this CTA's TMEM: no release before they finish
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
-template <int BN, bool FP8>
+template <int BN, bool FP8, bool PAIR>
 sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   static bool attr_set = false;
-  auto kern = gemm_tc_kernel<BN, FP8>;
+  auto kern = gemm_tc_kernel<BN, FP8, PAIR>;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm)");
     attr_set = true;
   }
-  const int tiles = prm.m_tiles * prm.n_tiles;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kThreads, C::kSmem, s>>>(g.ta, g.tw, g.tc, g.has_res ? g.tr : g.tc, prm);
-  cudaError_t e = cudaGetLastError();
+  const int items = PAIR ? ((prm.m_tiles + 1) / 2) * prm.n_tiles : prm.m_tiles * prm.n_tiles;
+  const int slots = PAIR ? num_sms() / 2 : num_sms();  // one CTA (PAIR: one two-CTA cluster) per SM (pair)
+  const int units = items < slots ? items : slots;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(unsigned(PAIR ? 2 * units : units), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const CUtensorMap& tr = g.has_res ? g.tr : g.tc;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, g.ta, g.tw, g.tc, tr, prm);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return SV_OK;
 }
@@ -441,24 +579,23 @@ sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int
                    box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Output-tile width: estimated main-loop time = waves x per-tile time. A tile's
-// K-step of 16 costs the larger of its tensor time (BN / 2 cycles at 8192
-// FLOP/clock/SM) and its operand traffic from L2, (128 + BN) x 32 bytes at
-// about 90 bytes/clock/SM (the L2 bandwidth measured under ncu: 16 TB/s at 61%
-// of its peak).
-int gemm_pick_bn(int M, int N, int K) {
+// Output-tile width: estimated time = waves x per-tile time, with the per-tile
+// time proportional to BN / (sustained TFLOP/s of that width). The rates are the
+// ones measured on GB300 for 23,328-row GEMMs with the copies and epilogue
+// running (TFLOP/s at 256 / 192 / 128 / 64 columns: about 1780 / 1480 / 1000 /
+// 600): wide tiles win whenever there are enough of them to fill the SMs.
+int gemm_pick_bn(int M, int N, int K, bool pair) {
   const int cand[4] = {256, 192, 128, 64};
+  const double rate[4] = {1780.0, 1480.0, 1000.0, 600.0};
   const int sms = num_sms() > 0 ? num_sms() : 148;
   int best = 256;
   double best_t = 1e30;
   const int mt = (M + kBM - 1) / kBM;
-  for (int bn : cand) {
-    const double mma = bn / 2.0;
-    const double l2 = (kBM + bn) * 32.0 / 90.0;
-    const double step = mma > l2 ? mma : l2;
-    const long tiles = long(mt) * ((N + bn - 1) / bn);
+  for (int i = 0; i < 4; ++i) {
+    const int bn = cand[i];
+    const long tiles = long(pair ? 2 * ((mt + 1) / 2) : mt) * ((N + bn - 1) / bn);
     const long waves = (tiles + sms - 1) / sms;
-    const double t = double(waves) * step * double((K + 15) / 16);
+    const double t = double(waves) * bn / rate[i] * double(K);
     if (t < best_t * 0.999) {
       best_t = t;
       best = bn;
@@ -472,10 +609,15 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
   g->N = N;
   g->K = K;
   g->fp8 = fp8;
-  g->bn = gemm_pick_bn(M, N, K);
+  // CTA pairs (256-row tiles, half the operand traffic per SM) pay off for long K,
+  // where A streams from DRAM (the MLP down-projection); short-K GEMMs run faster
+  // as independent CTAs (measured).
+  g->mc = (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && K >= 2048;
+  g->bn = gemm_pick_bn(M, N, K, g->mc);
+  if (g->mc && g->bn > kPairMaxBn) g->bn = kPairMaxBn;
   sv_status st = gemm_operand_map(&g->ta, A, M, K, fp8, kBM);
   if (st != SV_OK) return st;
-  return gemm_operand_map(&g->tw, W, N, K, fp8, g->bn);
+  return gemm_operand_map(&g->tw, W, N, K, fp8, g->mc ? g->bn / 2 : g->bn);
 }
 
 // Output (and residual) maps of a [M, N] row-major matrix in 32 x 32 blocks:
@@ -517,19 +659,33 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.pos = e.pos;
   p.pos_rows = e.pos_rows > 0 ? e.pos_rows : 1;
   p.has_res = e.residual != nullptr;
+  p.blk = static_cast<uint8_t*>(e.blk_out);
+  p.blk_T = e.blk_T;
+  p.blk_H = e.blk_H;
+  p.blk_B = e.blk_B;
+  p.blk_tiles = (e.blk_T + 127) / 128;
   p.act = e.act;
   p.out_e4m3 = e.out_e4m3;
   p.scale = e.scale;
   p.err = dev_err();
-  switch (g.bn | (g.fp8 ? 1 : 0)) {
-    case 256: return launch_bn<256, false>(g, p, s);
-    case 257: return launch_bn<256, true>(g, p, s);
-    case 192: return launch_bn<192, false>(g, p, s);
-    case 193: return launch_bn<192, true>(g, p, s);
-    case 128: return launch_bn<128, false>(g, p, s);
-    case 129: return launch_bn<128, true>(g, p, s);
-    case 64: return launch_bn<64, false>(g, p, s);
-    case 65: return launch_bn<64, true>(g, p, s);
+  const int key = g.bn | (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0);
+  switch (key) {
+    case 256: return launch_bn<256, false, false>(g, p, s);
+    case 257: return launch_bn<256, true, false>(g, p, s);
+    case 258: return launch_bn<256, false, true>(g, p, s);
+    case 259: return launch_bn<256, true, true>(g, p, s);
+    case 192: return launch_bn<192, false, false>(g, p, s);
+    case 193: return launch_bn<192, true, false>(g, p, s);
+    case 194: return launch_bn<192, false, true>(g, p, s);
+    case 195: return launch_bn<192, true, true>(g, p, s);
+    case 128: return launch_bn<128, false, false>(g, p, s);
+    case 129: return launch_bn<128, true, false>(g, p, s);
+    case 130: return launch_bn<128, false, true>(g, p, s);
+    case 131: return launch_bn<128, true, true>(g, p, s);
+    case 64: return launch_bn<64, false, false>(g, p, s);
+    case 65: return launch_bn<64, true, false>(g, p, s);
+    case 66: return launch_bn<64, false, true>(g, p, s);
+    case 67: return launch_bn<64, true, true>(g, p, s);
     default: set_error("gemm: no kernel for tile width %d", g.bn); return SV_ERR_UNSUPPORTED;
   }
 }

@@ -41,6 +41,10 @@ struct GemmEpi {
   int act = SV_ACT_NONE;
   int out_e4m3 = 0;
   float scale = 1.0f;
+  // Head-blocked output for attention (replaces the row-major store when set):
+  // see attention_blocked_bytes. `out` must still name a buffer of >= M*N f16.
+  void* blk_out = nullptr;
+  int blk_T = 0, blk_H = 0, blk_B = 0;
 };
 
 // The operand side of a GEMM: tensor maps for A and W plus the sizes.
@@ -49,6 +53,7 @@ struct GemmOperands {
   int M = 0, N = 0, K = 0;
   int fp8 = 0;
   int bn = 0;
+  int mc = 0;  // CTA pairs (clusters of 2) sharing one 256-row MMA
   int has_res = 0;
   const void* out = nullptr;  // epilogue buffers the output / residual maps describe
   const void* res = nullptr;
@@ -58,16 +63,22 @@ struct GemmOperands {
 // Tensor map of a K-major operand [rows, K] (row stride = K elements) with the
 // 128-byte swizzle the GEMM expects, box [box_rows, 128 bytes].
 sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int fp8, int box_rows);
-int gemm_pick_bn(int M, int N, int K);
+int gemm_pick_bn(int M, int N, int K, bool mc);
 sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8);
 // Builds the output / residual tensor maps for the epilogue's buffers (must precede gemm_launch).
 sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e);
 sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s);
 
 // ---- attention (attention.cu)
-// qkv: [B, T, 3*H*72] f16; o: [B, T, H*72] f16 / e4m3.
-sv_status attention_map(CUtensorMap* m, const void* qkv, int B, int T, int H);
-sv_status attention_launch(const CUtensorMap& m, void* o, int B, int T, int H, float scale, int out_e4m3,
+// Head-blocked Q/K/V: block (which, b, h, tile) at index ((which*B + b)*H + h)*tiles + tile
+// (which 0 = Q, 1 = K, 2 = V; tiles of 128 tokens), each block 9 column groups x 128 rows x
+// 8 f16 (2048 bytes per group: row r of group cg at cg*2048 + r*16). Rows past the last
+// token of an image are never written or read as data.
+size_t attention_blocked_bytes(int B, int T, int H);
+// Row-major [B, T, 3*H*72] f16 -> head-blocked.
+sv_status attention_repack_launch(const __half* qkv, void* blocked, int B, int T, int H, cudaStream_t s);
+// o: [B, T, H*72] f16 / e4m3.
+sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, float scale, int out_e4m3,
                            cudaStream_t s);
 
 // ---- elementwise (elementwise.cu)
