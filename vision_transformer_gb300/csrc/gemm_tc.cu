@@ -17,7 +17,8 @@
 //               (clusters of 2) that share one M = 256 MMA (cta_group::2):
 //               each CTA stages its 128 rows of A and half of the W tile, the
 //               leader issues the MMAs, each CTA's TMEM holds its 128 rows;
-//   warps 2..5  epilogue: tcgen05.ld of 32 columns at a time, fused math,
+//   warps 2..5  epilogue: tcgen05.ld of 32 columns at a time (the next
+//               chunk's load in flight during this chunk's math), fused math,
 //               the 32 x 32 result block staged in swizzled shared memory and
 //               written by a TMA store; residual blocks arrive by TMA one
 //               chunk ahead.
@@ -105,6 +106,15 @@ __device__ __forceinline__ void add8h(const uint4& v, float* f) {
     f[2 * i] += t.x;
     f[2 * i + 1] += t.y;
   }
+}
+
+// Bias of output columns n .. n+31 as four 8-column groups (zero past N or
+// without a bias; N is a multiple of 16).
+__device__ __forceinline__ void load_bias(const Params& p, int n, uint4 (&bq)[4]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    bq[g] = (p.bias && n + 8 * g < p.N) ? __ldg(reinterpret_cast<const uint4*>(p.bias + n + 8 * g))
+                                        : make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Number of 32-column chunks of tile column block nt that hold columns < N.
@@ -355,6 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = nt * BN;
       const int nch = tile_chunks(p, nt, BN);
       const uint32_t tbase = tmem_base + uint32_t(acc * BN) + (uint32_t(sub * 32) << 16);
+      // The TMEM load and the bias of chunk c + 1 are issued as soon as chunk c's
+      // accumulators are in registers, so their latency hides behind chunk c's math.
+      uint32_t r[32];
+      uint4 bq[4];
+      tmem_ld32(tbase, r);
+      load_bias(p, n0, bq);
 #pragma unroll 1
       for (int c = 0; c < nch; ++c, ++q) {
         const int b = q & 1;
@@ -367,22 +383,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (it2 < num_items) prefetch_item(it2, c2, q + 1);
         }
         const int n = n0 + 32 * c;
-        uint32_t r[32];
-        tmem_ld32(tbase + 32 * c, r);
-        tmem_ld_wait();
+        const int ngroups = min(4, (p.N - n) / 8);  // groups of 8 columns below N
+        tmem_ld_wait(r);
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * p.scale;
-        const int ngroups = min(4, (p.N - n) / 8);  // groups of 8 columns below N
-        if (p.bias) {
+        for (int g = 0; g < 4; ++g) {
+          const __half2* h = reinterpret_cast<const __half2*>(&bq[g]);
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            if (g < ngroups) {
-              float bb[8];
-              load8h(p.bias + n + 8 * g, bb);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[8 * g + i] += bb[i];
-            }
+          for (int i = 0; i < 4; ++i) {
+            const float2 t = __half22float2(h[i]);
+            v[8 * g + 2 * i] = fmaf(__uint_as_float(r[8 * g + 2 * i]), p.scale, t.x);
+            v[8 * g + 2 * i + 1] = fmaf(__uint_as_float(r[8 * g + 2 * i + 1]), p.scale, t.y);
+          }
+        }
+        if (c + 1 < nch) {
+          tmem_ld32(tbase + 32 * (c + 1), r);
+          load_bias(p, n + 32, bq);
         }
         if (p.pos) {
           const size_t poff = size_t(row % p.pos_rows) * size_t(p.N) + size_t(n);
@@ -475,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         mbar_arrive(bar_tempty + 8 * acc);
     }
+    tmem_ld_wait();  // a load of the next chunk may be in flight after an abort
     if (lane == 0) {
       bulk_wait_all();  // every store has read shared memory and written global memory
       for (int b = 0; b < 2; ++b)
