@@ -81,13 +81,16 @@ enum {
   kBarVFull = 5,    // +stage
   kBarVEmpty = 7,   // +stage
   kBarSFull = 9,    // +group
-  kBarSEmpty = 11,  // +group
+  kBarSEmpty = 11,  // +group: the group has read S into registers
   kBarPFull = 13,   // +group
-  kBarOFull = 15,   // +group
-  kBarOEmpty = 17,  // +group
-  kBarDrain = 19,
-  kNumBars = 20
+  kBarOFull = 15,   // +group: O += P V of the group's latest tile has finished
+  kBarDrain = 17,
+  kNumBars = 18
 };
+
+// The reference maximum of a row (log2 units) is raised only when a tile's
+// maximum exceeds it by more than this, so P <= 2^8 and O is rescaled rarely.
+constexpr float kSlack = 8.0f;
 
 __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -153,7 +156,6 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) 
       mbar_init(bar(kBarSEmpty + s), 128);  // every softmax thread of the group arrives
       mbar_init(bar(kBarPFull + s), 128);
       mbar_init(bar(kBarOFull + s), 1);
-      mbar_init(bar(kBarOEmpty + s), 128);
     }
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
@@ -216,25 +218,26 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) 
         if (w == 1) tc_commit(bar(kBarKEmpty + s));  // both groups have read K_j
         return true;
       };
-      auto issue_pv = [&](int w, int j) -> bool {  // O_w(j) = P_w(j) V_j
+      auto issue_pv = [&](int w, int j) -> bool {  // O_w += P_w(j) V_j
         const int s = j & 1;
         if (!mbar_wait(bar(kBarPFull + w), j & 1, abort_flag, p.err)) return false;
         if (!mbar_wait(bar(kBarVFull + s), (j >> 1) & 1, abort_flag, p.err)) return false;
-        if (!mbar_wait(bar(kBarOEmpty + w), (j & 1) ^ 1, abort_flag, p.err)) return false;
         tc_fence_after();
         const uint32_t pa = sbase + kOffP + w * kPBytes, va = sbase + kOffV + s * kOpBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // K = 128 keys in steps of 16
           mma_f16(tmem + uint32_t(256 + w * 128), make_sdesc(pa + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
-                  make_sdesc(va + kk * 256, 128, kGroupBytes, 0), idesc_o, kk > 0);
+                  make_sdesc(va + kk * 256, 128, kGroupBytes, 0), idesc_o, (j | kk) > 0);
         tc_commit(bar(kBarOFull + w));
         if (w == 1) tc_commit(bar(kBarVEmpty + s));  // both groups have read V_j
         return true;
       };
+      // S of the next tile is issued as soon as a group has read its S, so it is
+      // computed while that group's softmax of the current tile runs.
       bool ok = mbar_wait(bar(kBarQ), 0, abort_flag, p.err) && issue_s(0, 0) && issue_s(1, 0);
       for (int j = 0; ok && j < nkv; ++j) {
-        ok = issue_pv(0, j) && (j + 1 >= nkv || issue_s(0, j + 1)) && issue_pv(1, j) &&
-             (j + 1 >= nkv || issue_s(1, j + 1));
+        ok = (j + 1 >= nkv || issue_s(0, j + 1)) && (j + 1 >= nkv || issue_s(1, j + 1)) && issue_pv(0, j) &&
+             issue_pv(1, j);
       }
       tc_commit(bar(kBarDrain));
       mbar_wait_bounded(bar(kBarDrain), 0, p.err);
@@ -248,37 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) 
     const uint32_t o_tm = tmem + uint32_t(256 + w * 128) + lane_off;
     uint8_t* pbuf = smem + kOffP + w * kPBytes;
     const float sl2 = p.scale_log2;
-    float o[kDh];
-#pragma unroll
-    for (int d = 0; d < kDh; ++d) o[d] = 0.0f;
-    float m = -INFINITY;       // running max (log2 units) used for the newest P tile
-    float m_fold = -INFINITY;  // reference max of the accumulator o
-    float l = 0.0f;
+    // Reference maximum (log2 units) of this row's P tiles and of the O accumulator
+    // in TMEM; the softmax denominator accumulates in O's column 72.
+    float m = -INFINITY;
     bool ok = true;
-
-    // o = o * 2^(m_fold - m_i) + O(i) and l = l * 2^(m_fold - m_i) + rowsum(P(i)), with
-    // m_i = m (the max used for P(i)); the row sum is column 72 of O(i).
-    auto fold = [&](int i) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), i & 1, abort_flag, p.err))) return false;
-      tc_fence_after();
-      uint32_t a[32], c[32], e[16];
-      tmem_ld32(o_tm, a);
-      tmem_ld32(o_tm + 32, c);
-      tmem_ld16(o_tm + 64, e);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kBarOEmpty + w));
-      const float f = ex2(m_fold - m);
-#pragma unroll
-      for (int d = 0; d < 32; ++d) o[d] = fmaf(o[d], f, __uint_as_float(a[d]));
-#pragma unroll
-      for (int d = 0; d < 32; ++d) o[32 + d] = fmaf(o[32 + d], f, __uint_as_float(c[d]));
-#pragma unroll
-      for (int d = 0; d < 8; ++d) o[64 + d] = fmaf(o[64 + d], f, __uint_as_float(e[d]));
-      l = fmaf(l, f, __uint_as_float(e[8]));
-      m_fold = m;
-      return true;
-    };
 
     for (int j = 0; j < nkv && ok; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + w), j & 1, abort_flag, p.err))) {
@@ -286,48 +262,69 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) 
         break;
       }
       tc_fence_after();
+      // the whole S row in registers (four loads in flight), then S is released
+      uint32_t sv[4][32];
+      tmem_ld32(s_tm, sv[0]);
+      tmem_ld32(s_tm + 32, sv[1]);
+      tmem_ld32(s_tm + 64, sv[2]);
+      tmem_ld32(s_tm + 96, sv[3]);
+      tmem_ld_wait(sv[0]);
+      reg_fence(sv[1]);
+      reg_fence(sv[2]);
+      reg_fence(sv[3]);
+      tc_fence_before();
+      mbar_arrive(bar(kBarSEmpty + w));
       const int valid = T - j * kTile;  // keys of this tile that exist (>= 1)
-      // pass 1: row maximum over the existing keys
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(s_tm + 32 * c, v);
-        tmem_ld_wait();
-        if (valid >= kTile) {
+      if (valid < kTile) {              // keys past the last token: -inf, so P = 0 exactly
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
-        } else {
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (32 * c + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
+            if (32 * c + i >= valid) sv[c][i] = 0xff800000u;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) mx = fmax3(mx, __uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1]));
+      const float m_tile = mx * sl2;
+      const bool raise = m_tile > m + kSlack;  // always at j == 0
+      const float m_new = raise ? m_tile : m;
+      if (j > 0) {
+        // O += P(j-1) V has finished: the P buffer is free and O is stable
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), (j - 1) & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, raise)) {  // O (and its row sum) *= 2^(m - m_new), 1 for kept rows
+          const float f = ex2(m - m_new);
+#pragma unroll 1
+          for (int c = 0; c < 10; ++c) {  // 80 columns, 8 at a time (few live registers)
+            uint32_t e[8];
+            tmem_ld8(o_tm + 8 * c, e);
+            tmem_ld_wait();
+            asm volatile("" : "+r"(e[0]), "+r"(e[1]), "+r"(e[2]), "+r"(e[3]), "+r"(e[4]), "+r"(e[5]), "+r"(e[6]),
+                         "+r"(e[7]));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) e[i] = __float_as_uint(__uint_as_float(e[i]) * f);
+            tmem_st8(o_tm + 8 * c, e);
+          }
+          tmem_st_wait();
         }
       }
-      const float m_new = fmaxf(m, mx * sl2);
-      // O(j-1) is folded before P(j) overwrites the group's single P buffer
-      if (j >= 1 && !fold(j - 1)) {
-        ok = false;
-        break;
-      }
-      // pass 2: probabilities as the F16 P tile in shared memory
-#pragma unroll 1
+      m = m_new;
+      // P = 2^(scale log2(e) s - m) as the F16 P tile in shared memory
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(s_tm + 32 * c, v);
-        tmem_ld_wait();
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint4 wv;
           __half2* hw = reinterpret_cast<__half2*>(&wv);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int k0 = 32 * c + 8 * g + 2 * i;
-            float p0 = ex2(fmaf(__uint_as_float(v[8 * g + 2 * i]), sl2, -m_new));
-            float p1 = ex2(fmaf(__uint_as_float(v[8 * g + 2 * i + 1]), sl2, -m_new));
-            if (valid < kTile) {
-              p0 = k0 < valid ? p0 : 0.0f;
-              p1 = k0 + 1 < valid ? p1 : 0.0f;
-            }
+            const float p0 = ex2(fmaf(__uint_as_float(sv[c][8 * g + 2 * i]), sl2, -m));
+            const float p1 = ex2(fmaf(__uint_as_float(sv[c][8 * g + 2 * i + 1]), sl2, -m));
             hw[i] = __floats2half2_rn(p0, p1);
           }
           *reinterpret_cast<uint4*>(pbuf + (4 * c + g) * kGroupBytes + r * 16) = wv;
@@ -335,42 +332,60 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) 
       }
       tc_fence_before();
       fence_proxy_async_smem();  // P (generic-proxy stores) visible to the tensor core
-      mbar_arrive(bar(kBarSEmpty + w));
       mbar_arrive(bar(kBarPFull + w));
-      m = m_new;
     }
-    if (ok) ok = fold(nkv - 1);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), (nkv - 1) & 1, abort_flag, p.err));
 
     const int t = (2 * qpair + w) * kTile + r;
-    if (ok && t < T) {
-      const float inv = 1.0f / l;
-      const int D = p.H * kDh;
-      const size_t row = size_t(b) * size_t(T) + size_t(t);
-      if (!p.out_e4m3) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + row * size_t(D) + size_t(h) * kDh);
+    if (ok) {
+      tc_fence_after();
+      uint32_t a[32], c[32], e[16];
+      tmem_ld32(o_tm, a);
+      tmem_ld32(o_tm + 32, c);
+      tmem_ld16(o_tm + 64, e);
+      tmem_ld_wait(a);
+      reg_fence(c);
+      tmem_ld_wait();
+      float o[kDh];
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          uint4 wv;
-          __half2* hw = reinterpret_cast<__half2*>(&wv);
+      for (int d = 0; d < 32; ++d) o[d] = __uint_as_float(a[d]);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) hw[i] = __floats2half2_rn(o[8 * g + 2 * i] * inv, o[8 * g + 2 * i + 1] * inv);
-          dst[g] = wv;
-        }
-      } else {
-        uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * size_t(D) + size_t(h) * kDh);
+      for (int d = 0; d < 32; ++d) o[32 + d] = __uint_as_float(c[d]);
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          uint2 wv;
-          __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&wv);
+      for (int d = 0; d < 8; ++d) o[64 + d] = __uint_as_float(e[d]);
+      const float l = __uint_as_float(e[8]);
+      if (t < T) {
+        const float inv = 1.0f / l;
+        const int D = p.H * kDh;
+        const size_t row = size_t(b) * size_t(T) + size_t(t);
+        if (!p.out_e4m3) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + row * size_t(D) + size_t(h) * kDh);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            q[i] = __nv_cvt_float2_to_fp8x2(
-                make_float2(16.0f * o[8 * g + 2 * i] * inv, 16.0f * o[8 * g + 2 * i + 1] * inv), __NV_SATFINITE,
-                __NV_E4M3);
-          dst[g] = wv;
+          for (int g = 0; g < kGroups; ++g) {
+            uint4 wv;
+            __half2* hw = reinterpret_cast<__half2*>(&wv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              hw[i] = __floats2half2_rn(o[8 * g + 2 * i] * inv, o[8 * g + 2 * i + 1] * inv);
+            dst[g] = wv;
+          }
+        } else {
+          uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * size_t(D) + size_t(h) * kDh);
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) {
+            uint2 wv;
+            __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&wv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              q[i] = __nv_cvt_float2_to_fp8x2(
+                  make_float2(16.0f * o[8 * g + 2 * i] * inv, 16.0f * o[8 * g + 2 * i + 1] * inv), __NV_SATFINITE,
+                  __NV_E4M3);
+            dst[g] = wv;
+          }
         }
       }
     }
+    tmem_ld_wait();
   }
   __syncthreads();
   if (warp == 1) {
