@@ -51,15 +51,22 @@ constexpr int kGroupBytes = kTile * 16;      // 2048: one column group of a tile
 constexpr int kBlockBytes = kGroups * kGroupBytes;  // 18432: one operand tile in memory
 constexpr int kOpBytes = 10 * kGroupBytes;   // 80 columns in shared memory (72 + zero pad)
 constexpr int kPBytes = 16 * kGroupBytes;    // 128 keys of probabilities
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kBarBytes = 320;  // barriers, TMEM address slot, abort flag
 
-// Shared memory map (offsets from the 1024-aligned base).
-constexpr int kOffQ = 0;                     // 2 query tiles
-constexpr int kOffK = kOffQ + 2 * kOpBytes;  // 2 stages
-constexpr int kOffV = kOffK + 2 * kOpBytes;  // 2 stages
-constexpr int kOffP = kOffV + 2 * kOpBytes;  // one buffer per softmax group
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kSmem = 1024 + kOffBar + 256;
+// Shared memory map (offsets from the 1024-aligned base) for QB query buffers
+// (of two tiles each), KS key stages and VS value stages.
+template <int QB, int KS, int VS>
+struct Smem {
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * QB * kOpBytes;
+  static constexpr int kOffV = kOffK + KS * kOpBytes;
+  static constexpr int kOffP = kOffV + VS * kOpBytes;  // one buffer per softmax group
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kBytes = 1024 + kOffBar + kBarBytes;
+  static_assert(kBytes <= 232448, "shared memory budget");
+  static_assert(QB >= 1 && QB <= 2 && KS >= 2 && KS <= 4 && VS >= 2 && VS <= 4, "buffer counts");
+};
 
 // TMEM columns: S_w at 128 w, O_w at 256 + 128 w.
 constexpr uint32_t kTmemCols = 512;
@@ -75,22 +82,29 @@ struct Params {
 
 // Barrier indices (8 bytes each).
 enum {
-  kBarQ = 0,
-  kBarKFull = 1,    // +stage
-  kBarKEmpty = 3,   // +stage
-  kBarVFull = 5,    // +stage
-  kBarVEmpty = 7,   // +stage
-  kBarSFull = 9,    // +group
-  kBarSEmpty = 11,  // +group: the group has read S into registers
-  kBarPFull = 13,   // +group
-  kBarOFull = 15,   // +group: O += P V of the group's latest tile has finished
-  kBarDrain = 17,
-  kNumBars = 18
+  kBarQFull = 0,    // +buffer
+  kBarQEmpty = 2,   // +buffer: both groups' last S product of the item has finished
+  kBarKFull = 4,    // +stage
+  kBarKEmpty = 8,   // +stage
+  kBarVFull = 12,   // +stage
+  kBarVEmpty = 16,  // +stage
+  kBarSFull = 20,   // +group
+  kBarSEmpty = 22,  // +group: the group has read S into registers
+  kBarPFull = 24,   // +2 group + half: that half of the group's P tile is written
+  kBarPEmpty = 28,  // +2 group + half: O += P V of that half has finished
+  kBarOFull = 32,   // +group: O += P V of the group's latest tile has finished
+  kBarOEmpty = 34,  // +group: the group has read the item's final O
+  kBarDrain = 36,   // +group
+  kNumBars = 38
 };
+static_assert(8 * kNumBars + 8 <= kBarBytes, "barrier area");
 
 // The reference maximum of a row (log2 units) is raised only when a tile's
 // maximum exceeds it by more than this, so P <= 2^8 and O is rescaled rarely.
 constexpr float kSlack = 8.0f;
+
+// Zeros for the rows of a partial V tile past the last token.
+__device__ __align__(128) uint8_t g_zero_rows[kGroupBytes];
 
 __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -114,11 +128,48 @@ __device__ __forceinline__ uint32_t copy_tile(uint32_t dst, const uint8_t* src, 
   return uint32_t(kGroups * rows * 16);
 }
 
+// As copy_tile, and the rows past the last token are filled with zeros (a V tile:
+// its masked keys have P = 0, and 0 times a zero row stays 0 whatever the buffer
+// held before).
+__device__ __forceinline__ uint32_t copy_tile_zero_tail(uint32_t dst, const uint8_t* src, int rows, uint32_t bar) {
+  if (rows == kTile) {
+    bulk_copy(dst, src, kBlockBytes, bar);
+    return kBlockBytes;
+  }
+  for (int g = 0; g < kGroups; ++g) {
+    bulk_copy(dst + g * kGroupBytes, src + g * kGroupBytes, rows * 16, bar);
+    bulk_copy(dst + g * kGroupBytes + rows * 16, g_zero_rows, (kTile - rows) * 16, bar);
+  }
+  return kBlockBytes;
+}
+
 __device__ __forceinline__ uint32_t tile_bytes(int rows) {
   return rows == kTile ? uint32_t(kBlockBytes) : uint32_t(kGroups * rows * 16);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) {
+// Work item -> (query pair, head, image); the query pairs of one (image, head)
+// are consecutive items, so CTAs running at the same time share K and V in L2.
+struct Item {
+  int qp, h, b;
+};
+__device__ __forceinline__ Item item_of(int it, int nq, int H) {
+  Item r;
+  r.qp = it % nq;
+  const int bh = it / nq;
+  r.h = bh % H;
+  r.b = bh / H;
+  return r;
+}
+
+// Persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...
+// The K / V stream and the softmax pipeline run on across item boundaries; Q is
+// double buffered so the next item's queries arrive during the current item.
+template <int QB, int KS, int VS>
+// 11 warps: three share each of three SM sub-partitions, so a thread may hold at most
+// 16384 / (3 x 32) registers, rounded down to the allocation granule.
+__global__ void __maxnreg__(168) attention_kernel(const Params p) {
+  using L = Smem<QB, KS, VS>;
+  constexpr int kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffP = L::kOffP, kOffBar = L::kOffBar;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -128,36 +179,51 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) 
   auto bar = [&](int i) { return bar0 + 8u * uint32_t(i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qpair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int T = p.T;
   const int nkv = (T + kTile - 1) / kTile;
-  // operand block of (which, tile) for this image and head
-  auto block = [&](int which, int tile) {
+  const int nq = (T + 2 * kTile - 1) / (2 * kTile);
+  const int items = nq * p.H * p.B;
+  const int n_my = int(blockIdx.x) < items ? (items - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
+  const int total = n_my * nkv;  // kv tiles this CTA walks, over all its items
+  // operand block of (which, image, head, tile)
+  auto block = [&](int which, int b, int h, int tile) {
     return p.blocked + (((size_t(which) * p.B + b) * p.H + h) * p.tiles + tile) * size_t(kBlockBytes);
   };
 
   // Zero every operand buffer (Q, K and V tiles including their pad column group),
   // except V's pad group, whose first column is 1: P V then carries the row sum
   // of P (the softmax denominator, from the same F16 P) in output column 72.
-  for (int i = threadIdx.x; i < (6 * kOpBytes) / 16; i += kThreads) {
+  for (int i = threadIdx.x; i < kOffP / 16; i += kThreads) {
     const int off = i * 16;
     const bool v_pad = off >= kOffV && ((off - kOffV) % kOpBytes) >= kGroups * kGroupBytes;
     reinterpret_cast<uint4*>(smem)[i] = make_uint4(v_pad ? 0x3C00u : 0u, 0, 0, 0);
   }
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
-    mbar_init(bar(kBarQ), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < QB; ++s) {
+      mbar_init(bar(kBarQFull + s), 1);
+      mbar_init(bar(kBarQEmpty + s), 2);  // one release per group
+    }
+    for (int s = 0; s < KS; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
-      mbar_init(bar(kBarKEmpty + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 2);
+    }
+    for (int s = 0; s < VS; ++s) {
       mbar_init(bar(kBarVFull + s), 1);
-      mbar_init(bar(kBarVEmpty + s), 1);
-      mbar_init(bar(kBarSFull + s), 1);
-      mbar_init(bar(kBarSEmpty + s), 128);  // every softmax thread of the group arrives
-      mbar_init(bar(kBarPFull + s), 128);
-      mbar_init(bar(kBarOFull + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 2);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(bar(kBarSFull + w), 1);
+      mbar_init(bar(kBarSEmpty + w), 128);  // every softmax thread of the group arrives
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(bar(kBarPFull + 2 * w + h), 128);
+        mbar_init(bar(kBarPEmpty + 2 * w + h), 1);
+      }
+      mbar_init(bar(kBarOFull + w), 1);
+      mbar_init(bar(kBarOEmpty + w), 128);
     }
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain + 1), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -172,78 +238,105 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) 
 
   if (warp == 0) {
     if (lane == 0) {
-      // both query tiles on one barrier
-      const int qr0 = tile_rows(T, 2 * qpair), qr1 = tile_rows(T, 2 * qpair + 1);
-      mbar_arrive_expect_tx(bar(kBarQ), tile_bytes(qr0) + (qr1 ? tile_bytes(qr1) : 0));
-      copy_tile(sbase + kOffQ, block(0, 2 * qpair), qr0, bar(kBarQ));
-      if (qr1) copy_tile(sbase + kOffQ + kOpBytes, block(0, 2 * qpair + 1), qr1, bar(kBarQ));
-      uint32_t issued = 0, issued_phase = 0;  // bit s: K stage s; bit 2+s: V stage s
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        const int rows = tile_rows(T, j);
-        if (!mbar_wait(bar(kBarKEmpty + s), ph ^ 1, abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(bar(kBarKFull + s), tile_bytes(rows));
-        copy_tile(sbase + kOffK + s * kOpBytes, block(1, j), rows, bar(kBarKFull + s));
-        issued |= 1u << s;
-        issued_phase = (issued_phase & ~(1u << s)) | (ph << s);
-        if (!mbar_wait(bar(kBarVEmpty + s), ph ^ 1, abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(bar(kBarVFull + s), tile_bytes(rows));
-        copy_tile(sbase + kOffV + s * kOpBytes, block(2, j), rows, bar(kBarVFull + s));
-        issued |= 1u << (2 + s);
-        issued_phase = (issued_phase & ~(1u << (2 + s))) | (ph << (2 + s));
+      // copies in flight per full barrier (bit b: Q buffer b, 4 + K stage, 8 + V stage) and their phase bit
+      uint32_t issued = 0, issued_phase = 0;
+      auto note = [&](int bit, uint32_t ph) {
+        issued |= 1u << bit;
+        issued_phase = (issued_phase & ~(1u << bit)) | (ph << bit);
+      };
+      bool ok = true;
+      for (int n = 0; n < n_my && ok; ++n) {
+        const Item I = item_of(int(blockIdx.x) + n * int(gridDim.x), nq, p.H);
+        const int qb = n % QB;
+        const uint32_t qph = (n / QB) & 1;
+        if (!mbar_wait(bar(kBarQEmpty + qb), qph ^ 1, abort_flag, p.err)) break;
+        const int qr0 = tile_rows(T, 2 * I.qp), qr1 = tile_rows(T, 2 * I.qp + 1);
+        mbar_arrive_expect_tx(bar(kBarQFull + qb), tile_bytes(qr0) + (qr1 ? tile_bytes(qr1) : 0));
+        copy_tile(sbase + kOffQ + (2 * qb) * kOpBytes, block(0, I.b, I.h, 2 * I.qp), qr0, bar(kBarQFull + qb));
+        if (qr1)
+          copy_tile(sbase + kOffQ + (2 * qb + 1) * kOpBytes, block(0, I.b, I.h, 2 * I.qp + 1), qr1,
+                    bar(kBarQFull + qb));
+        note(qb, qph);
+        for (int j = 0; j < nkv; ++j) {
+          const int t = n * nkv + j, ks = t % KS, vs = t % VS;
+          const uint32_t kph = (t / KS) & 1, vph = (t / VS) & 1;
+          const int rows = tile_rows(T, j);
+          if (!mbar_wait(bar(kBarKEmpty + ks), kph ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarKFull + ks), tile_bytes(rows));
+          copy_tile(sbase + kOffK + ks * kOpBytes, block(1, I.b, I.h, j), rows, bar(kBarKFull + ks));
+          note(4 + ks, kph);
+          if (!mbar_wait(bar(kBarVEmpty + vs), vph ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarVFull + vs), kBlockBytes);
+          copy_tile_zero_tail(sbase + kOffV + vs * kOpBytes, block(2, I.b, I.h, j), rows, bar(kBarVFull + vs));
+          note(8 + vs, vph);
+        }
       }
       // every copy this thread issued lands before the CTA can exit
-      mbar_wait_bounded(bar(kBarQ), 0, p.err);
-      for (int s = 0; s < 2; ++s) {
-        if (issued & (1u << s)) mbar_wait_bounded(bar(kBarKFull + s), (issued_phase >> s) & 1, p.err);
-        if (issued & (4u << s)) mbar_wait_bounded(bar(kBarVFull + s), (issued_phase >> (2 + s)) & 1, p.err);
+      for (int i = 0; i < 12; ++i) {
+        const int fb = i < 4 ? kBarQFull + i : (i < 8 ? kBarKFull + i - 4 : kBarVFull + i - 8);
+        if (issued & (1u << i)) mbar_wait_bounded(bar(fb), (issued_phase >> i) & 1, p.err);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp <= 2) {
     if (lane == 0) {
+      // MMA issuer of softmax group w = warp - 1, in the group's own order: S(0); then per
+      // tile t (item t / nkv, key tile t % nkv): S(t+1) once K_{t+1} (and, on an item's
+      // first tile, its Q) is in and the group has read S(t) from TMEM; O += P V for
+      // each 64-key half of P(t) once that half is written, V_t is in and (an item's
+      // first tile) the group has read the previous item's O.
+      const int w = warp - 1;
       constexpr uint32_t idesc_s = make_idesc(128, 128, 0, false);  // S = Q K^T, both K-major
       constexpr uint32_t idesc_o = make_idesc(128, 80, 0, true);    // O = P V, V MN-major
-      auto issue_s = [&](int w, int j) -> bool {  // S_w(j) = Q_w K_j^T
-        const int s = j & 1;
-        if (!mbar_wait(bar(kBarKFull + s), (j >> 1) & 1, abort_flag, p.err)) return false;
-        if (!mbar_wait(bar(kBarSEmpty + w), (j & 1) ^ 1, abort_flag, p.err)) return false;
+      auto issue_s = [&](int t) -> bool {
+        const int n = t / nkv, j = t - n * nkv;
+        if (!mbar_wait(bar(kBarKFull + t % KS), (t / KS) & 1, abort_flag, p.err)) return false;
+        if (!mbar_wait(bar(kBarSEmpty + w), (t & 1) ^ 1, abort_flag, p.err)) return false;
+        if (j == 0 && !mbar_wait(bar(kBarQFull + n % QB), (n / QB) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
-        const uint32_t qa = sbase + kOffQ + w * kOpBytes, ka = sbase + kOffK + s * kOpBytes;
+        const uint32_t qa = sbase + kOffQ + (2 * (n % QB) + w) * kOpBytes, ka = sbase + kOffK + (t % KS) * kOpBytes;
 #pragma unroll
         for (int kk = 0; kk < 5; ++kk)  // K = 80 in steps of 16 (two column groups)
           mma_f16(tmem + uint32_t(w * 128), make_sdesc(qa + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
                   make_sdesc(ka + kk * 2 * kGroupBytes, kGroupBytes, 128, 0), idesc_s, kk > 0);
         tc_commit(bar(kBarSFull + w));
-        if (w == 1) tc_commit(bar(kBarKEmpty + s));  // both groups have read K_j
+        tc_commit(bar(kBarKEmpty + t % KS));
+        if (j == nkv - 1) tc_commit(bar(kBarQEmpty + n % QB));
         return true;
       };
-      auto issue_pv = [&](int w, int j) -> bool {  // O_w += P_w(j) V_j
-        const int s = j & 1;
-        if (!mbar_wait(bar(kBarPFull + w), j & 1, abort_flag, p.err)) return false;
-        if (!mbar_wait(bar(kBarVFull + s), (j >> 1) & 1, abort_flag, p.err)) return false;
+      auto issue_pv = [&](int u, int half) -> bool {
+        const int n = u / nkv, j = u - n * nkv;
+        if (!mbar_wait(bar(kBarPFull + 2 * w + half), u & 1, abort_flag, p.err)) return false;
+        if (!mbar_wait(bar(kBarVFull + u % VS), (u / VS) & 1, abort_flag, p.err)) return false;
+        if (j == 0 && half == 0 && n > 0 && !mbar_wait(bar(kBarOEmpty + w), (n - 1) & 1, abort_flag, p.err))
+          return false;
         tc_fence_after();
-        const uint32_t pa = sbase + kOffP + w * kPBytes, va = sbase + kOffV + s * kOpBytes;
+        const uint32_t pa = sbase + kOffP + w * kPBytes + half * (kPBytes / 2),
+                       va = sbase + kOffV + (u % VS) * kOpBytes + half * 4 * 256;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // K = 128 keys in steps of 16
+        for (int kk = 0; kk < 4; ++kk)  // K = 64 keys in steps of 16
           mma_f16(tmem + uint32_t(256 + w * 128), make_sdesc(pa + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
-                  make_sdesc(va + kk * 256, 128, kGroupBytes, 0), idesc_o, (j | kk) > 0);
-        tc_commit(bar(kBarOFull + w));
-        if (w == 1) tc_commit(bar(kBarVEmpty + s));  // both groups have read V_j
+                  make_sdesc(va + kk * 256, 128, kGroupBytes, 0), idesc_o, (j | half | kk) > 0);
+        tc_commit(bar(kBarPEmpty + 2 * w + half));
+        if (half) {
+          tc_commit(bar(kBarOFull + w));
+          tc_commit(bar(kBarVEmpty + u % VS));
+        }
         return true;
       };
-      // S of the next tile is issued as soon as a group has read its S, so it is
-      // computed while that group's softmax of the current tile runs.
-      bool ok = mbar_wait(bar(kBarQ), 0, abort_flag, p.err) && issue_s(0, 0) && issue_s(1, 0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        ok = (j + 1 >= nkv || issue_s(0, j + 1)) && (j + 1 >= nkv || issue_s(1, j + 1)) && issue_pv(0, j) &&
-             issue_pv(1, j);
-      }
-      tc_commit(bar(kBarDrain));
-      mbar_wait_bounded(bar(kBarDrain), 0, p.err);
+      bool ok = total == 0 || issue_s(0);
+      for (int t = 0; ok && t < total; ++t)
+        ok = (t + 1 >= total || issue_s(t + 1)) && issue_pv(t, 0) && issue_pv(t, 1);
+      tc_commit(bar(kBarDrain + w));
+      mbar_wait_bounded(bar(kBarDrain + w), 0, p.err);
     }
   } else {
-    const int w = (warp - 2) >> 2;  // softmax group
+    const int w = (warp - 3) >> 2;  // softmax group
     const int sub = warp & 3;       // TMEM lane quarter
     const int r = sub * 32 + lane;  // query row within the group's tile == TMEM lane
     const uint32_t lane_off = uint32_t(sub * 32) << 16;
@@ -256,8 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) 
     float m = -INFINITY;
     bool ok = true;
 
-    for (int j = 0; j < nkv && ok; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + w), j & 1, abort_flag, p.err))) {
+    for (int t = 0; t < total && ok; ++t) {
+      const int n = t / nkv, j = t - n * nkv;
+      if (j == 0) m = -INFINITY;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + w), t & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -282,105 +377,119 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const Params p) 
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= valid) sv[c][i] = 0xff800000u;
       }
-      float mx = -INFINITY;
+      // row maximum: four independent chains, then combined
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) mx = fmax3(mx, __uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1]));
+        for (int i = 0; i < 32; i += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mq[k] = fmax3(mq[k], __uint_as_float(sv[c][i + 2 * k]), __uint_as_float(sv[c][i + 2 * k + 1]));
+      const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
       const float m_tile = mx * sl2;
-      const bool raise = m_tile > m + kSlack;  // always at j == 0
+      const bool raise = m_tile > m + kSlack;  // always on an item's first tile
       const float m_new = raise ? m_tile : m;
-      if (j > 0) {
-        // O += P(j-1) V has finished: the P buffer is free and O is stable
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), (j - 1) & 1, abort_flag, p.err))) {
+      if (j > 0 && __any_sync(0xffffffffu, raise)) {
+        // O (and its row sum) *= 2^(m - m_new), 1 for kept rows, once O += P(t-1) V has finished
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), (t - 1) & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, raise)) {  // O (and its row sum) *= 2^(m - m_new), 1 for kept rows
-          const float f = ex2(m - m_new);
+        const float f = ex2(m - m_new);
 #pragma unroll 1
-          for (int c = 0; c < 10; ++c) {  // 80 columns, 8 at a time (few live registers)
-            uint32_t e[8];
-            tmem_ld8(o_tm + 8 * c, e);
-            tmem_ld_wait();
-            asm volatile("" : "+r"(e[0]), "+r"(e[1]), "+r"(e[2]), "+r"(e[3]), "+r"(e[4]), "+r"(e[5]), "+r"(e[6]),
-                         "+r"(e[7]));
+        for (int c = 0; c < 10; ++c) {  // 80 columns, 8 at a time (few live registers)
+          uint32_t e[8];
+          tmem_ld8(o_tm + 8 * c, e);
+          tmem_ld_wait();
+          asm volatile("" : "+r"(e[0]), "+r"(e[1]), "+r"(e[2]), "+r"(e[3]), "+r"(e[4]), "+r"(e[5]), "+r"(e[6]),
+                       "+r"(e[7]));
 #pragma unroll
-            for (int i = 0; i < 8; ++i) e[i] = __float_as_uint(__uint_as_float(e[i]) * f);
-            tmem_st8(o_tm + 8 * c, e);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 8; ++i) e[i] = __float_as_uint(__uint_as_float(e[i]) * f);
+          tmem_st8(o_tm + 8 * c, e);
         }
+        tmem_st_wait();
       }
       m = m_new;
-      // P = 2^(scale log2(e) s - m) as the F16 P tile in shared memory
+      // P = 2^(scale log2(e) s - m) as F16, in two halves of 64 keys; a half's buffer
+      // is free once O += P V of the same half of the previous tile has finished
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint4 wv;
-          __half2* hw = reinterpret_cast<__half2*>(&wv);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(sv[c][8 * g + 2 * i]), sl2, -m));
-            const float p1 = ex2(fmaf(__uint_as_float(sv[c][8 * g + 2 * i + 1]), sl2, -m));
-            hw[i] = __floats2half2_rn(p0, p1);
-          }
-          *reinterpret_cast<uint4*>(pbuf + (4 * c + g) * kGroupBytes + r * 16) = wv;
+      for (int half = 0; half < 2; ++half) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarPEmpty + 2 * w + half), (t & 1) ^ 1, abort_flag, p.err))) {
+          ok = false;
+          break;
         }
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();  // P (generic-proxy stores) visible to the tensor core
-      mbar_arrive(bar(kBarPFull + w));
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), (nkv - 1) & 1, abort_flag, p.err));
-
-    const int t = (2 * qpair + w) * kTile + r;
-    if (ok) {
-      tc_fence_after();
-      uint32_t a[32], c[32], e[16];
-      tmem_ld32(o_tm, a);
-      tmem_ld32(o_tm + 32, c);
-      tmem_ld16(o_tm + 64, e);
-      tmem_ld_wait(a);
-      reg_fence(c);
-      tmem_ld_wait();
-      float o[kDh];
+        uint8_t* ph = pbuf + half * (kPBytes / 2);
 #pragma unroll
-      for (int d = 0; d < 32; ++d) o[d] = __uint_as_float(a[d]);
+        for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-      for (int d = 0; d < 32; ++d) o[32 + d] = __uint_as_float(c[d]);
-#pragma unroll
-      for (int d = 0; d < 8; ++d) o[64 + d] = __uint_as_float(e[d]);
-      const float l = __uint_as_float(e[8]);
-      if (t < T) {
-        const float inv = 1.0f / l;
-        const int D = p.H * kDh;
-        const size_t row = size_t(b) * size_t(T) + size_t(t);
-        if (!p.out_e4m3) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + row * size_t(D) + size_t(h) * kDh);
-#pragma unroll
-          for (int g = 0; g < kGroups; ++g) {
+          for (int g = 0; g < 4; ++g) {
             uint4 wv;
             __half2* hw = reinterpret_cast<__half2*>(&wv);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              hw[i] = __floats2half2_rn(o[8 * g + 2 * i] * inv, o[8 * g + 2 * i + 1] * inv);
-            dst[g] = wv;
+            for (int i = 0; i < 4; ++i) {
+              const float p0 = ex2(fmaf(__uint_as_float(sv[2 * half + cc][8 * g + 2 * i]), sl2, -m));
+              const float p1 = ex2(fmaf(__uint_as_float(sv[2 * half + cc][8 * g + 2 * i + 1]), sl2, -m));
+              hw[i] = __floats2half2_rn(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(ph + (4 * cc + g) * kGroupBytes + r * 16) = wv;
           }
-        } else {
-          uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * size_t(D) + size_t(h) * kDh);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();  // P (generic-proxy stores) visible to the tensor core
+        mbar_arrive(bar(kBarPFull + 2 * w + half));
+      }
+      if (!ok) break;
+
+      if (j == nkv - 1) {  // the item's last tile: O / row sum -> output rows
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), t & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t a[32], c[32], e[16];
+        tmem_ld32(o_tm, a);
+        tmem_ld32(o_tm + 32, c);
+        tmem_ld16(o_tm + 64, e);
+        tmem_ld_wait(a);
+        reg_fence(c);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarOEmpty + w));  // the next item's first P V may overwrite O
+        const Item I = item_of(int(blockIdx.x) + n * int(gridDim.x), nq, p.H);
+        const int tq = (2 * I.qp + w) * kTile + r;
+        if (tq < T) {
+          const float inv = 1.0f / __uint_as_float(e[8]);
+          const int D = p.H * kDh;
+          const size_t row = size_t(I.b) * size_t(T) + size_t(tq);
+          if (!p.out_e4m3) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + row * size_t(D) + size_t(I.h) * kDh);
 #pragma unroll
-          for (int g = 0; g < kGroups; ++g) {
-            uint2 wv;
-            __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&wv);
+            for (int g = 0; g < kGroups; ++g) {
+              const uint32_t* src = g < 4 ? a + 8 * g : (g < 8 ? c + 8 * (g - 4) : e);
+              uint4 wv;
+              __half2* hw = reinterpret_cast<__half2*>(&wv);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              q[i] = __nv_cvt_float2_to_fp8x2(
-                  make_float2(16.0f * o[8 * g + 2 * i] * inv, 16.0f * o[8 * g + 2 * i + 1] * inv), __NV_SATFINITE,
-                  __NV_E4M3);
-            dst[g] = wv;
+              for (int i = 0; i < 4; ++i)
+                hw[i] = __floats2half2_rn(__uint_as_float(src[2 * i]) * inv, __uint_as_float(src[2 * i + 1]) * inv);
+              dst[g] = wv;
+            }
+          } else {
+            uint2* dst =
+                reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * size_t(D) + size_t(I.h) * kDh);
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g) {
+              const uint32_t* src = g < 4 ? a + 8 * g : (g < 8 ? c + 8 * (g - 4) : e);
+              uint2 wv;
+              __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&wv);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                q[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * __uint_as_float(src[2 * i]) * inv,
+                                                            16.0f * __uint_as_float(src[2 * i + 1]) * inv),
+                                                __NV_SATFINITE, __NV_E4M3);
+              dst[g] = wv;
+            }
           }
         }
       }
@@ -410,6 +519,26 @@ __global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restric
       *reinterpret_cast<const uint4*>(qkv + m * 3 * D + col);
 }
 
+// Buffer configuration: 0 = two Q buffers, 2 + 2 K / V stages; 1 = one Q buffer,
+// 3 + 3 stages; 2 = one Q buffer, 4 K + 2 V stages.
+int g_attention_config = 0;
+int attention_config() { return g_attention_config; }
+
+template <int QB, int KS, int VS>
+sv_status attention_launch_cfg(const Params& p, int grid, cudaStream_t s) {
+  static bool attr_set = false;
+  auto kern = attention_kernel<QB, KS, VS>;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<QB, KS, VS>::kBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
+    attr_set = true;
+  }
+  kern<<<unsigned(grid), kThreads, Smem<QB, KS, VS>::kBytes, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return SV_OK;
+}
+
 }  // namespace
 
 size_t attention_blocked_bytes(int B, int T, int H) {
@@ -426,12 +555,6 @@ sv_status attention_repack_launch(const __half* qkv, void* blocked, int B, int T
 
 sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, float scale, int out_e4m3,
                            cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
-    attr_set = true;
-  }
   Params p;
   p.blocked = static_cast<const uint8_t*>(blocked);
   p.B = B;
@@ -442,11 +565,14 @@ sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, fl
   p.out = o;
   p.out_e4m3 = out_e4m3;
   p.err = dev_err();
-  dim3 grid((T + 2 * kTile - 1) / (2 * kTile), H, B);
-  attention_kernel<<<grid, kThreads, kSmem, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
-  return SV_OK;
+  const int items = ((T + 2 * kTile - 1) / (2 * kTile)) * H * B;
+  const int sms = num_sms() > 0 ? num_sms() : 1;
+  const int grid = items < sms ? items : sms;
+  switch (attention_config()) {
+    case 1: return attention_launch_cfg<1, 3, 3>(p, grid, s);
+    case 2: return attention_launch_cfg<1, 4, 2>(p, grid, s);
+    default: return attention_launch_cfg<2, 2, 2>(p, grid, s);
+  }
 }
 
 }  // namespace sv
