@@ -38,6 +38,8 @@
 //               core serves the other.
 #include <cuda_fp8.h>
 
+#include <cstring>
+
 #include "ptx.cuh"
 #include "sv_internal.h"
 
@@ -52,7 +54,7 @@ constexpr int kBlockBytes = kGroups * kGroupBytes;  // 18432: one operand tile i
 constexpr int kOpBytes = 10 * kGroupBytes;   // 80 columns in shared memory (72 + zero pad)
 constexpr int kPBytes = 16 * kGroupBytes;    // 128 keys of probabilities
 constexpr int kThreads = 352;
-constexpr int kBarBytes = 320;  // barriers, TMEM address slot, abort flag
+constexpr int kBarBytes = 384;  // barriers, TMEM address slot, abort flag
 
 // Shared memory map (offsets from the 1024-aligned base) for QB query buffers
 // (of two tiles each), KS key stages and VS value stages.
@@ -95,13 +97,15 @@ enum {
   kBarOFull = 32,   // +group: O += P V of the group's latest tile has finished
   kBarOEmpty = 34,  // +group: the group has read the item's final O
   kBarDrain = 36,   // +group
-  kNumBars = 38
+  kBarStage = 38,   // +group: every warp's output store has read its staging rows
+  kNumBars = 40
 };
 static_assert(8 * kNumBars + 8 <= kBarBytes, "barrier area");
 
 // The reference maximum of a row (log2 units) is raised only when a tile's
-// maximum exceeds it by more than this, so P <= 2^8 and O is rescaled rarely.
-constexpr float kSlack = 8.0f;
+// maximum exceeds it by more than this: P <= 2^15 stays finite in F16 (whose
+// relative precision does not depend on the magnitude), and O is rescaled rarely.
+constexpr float kSlack = 15.0f;
 
 // Zeros for the rows of a partial V tile past the last token.
 __device__ __align__(128) uint8_t g_zero_rows[kGroupBytes];
@@ -167,7 +171,7 @@ __device__ __forceinline__ Item item_of(int it, int nq, int H) {
 template <int QB, int KS, int VS>
 // 11 warps: three share each of three SM sub-partitions, so a thread may hold at most
 // 16384 / (3 x 32) registers, rounded down to the allocation granule.
-__global__ void __maxnreg__(168) attention_kernel(const Params p) {
+__global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtensorMap tm_out, const Params p) {
   using L = Smem<QB, KS, VS>;
   constexpr int kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffP = L::kOffP, kOffBar = L::kOffBar;
   extern __shared__ uint8_t smem_raw[];
@@ -224,6 +228,8 @@ __global__ void __maxnreg__(168) attention_kernel(const Params p) {
     }
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrain + 1), 1);
+    mbar_init(bar(kBarStage), 4);  // one arrival per warp of the group
+    mbar_init(bar(kBarStage + 1), 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -344,10 +350,77 @@ __global__ void __maxnreg__(168) attention_kernel(const Params p) {
     const uint32_t o_tm = tmem + uint32_t(256 + w * 128) + lane_off;
     uint8_t* pbuf = smem + kOffP + w * kPBytes;
     const float sl2 = p.scale_log2;
+    const int D = p.H * kDh;
+    // An item's output rows: the final O (with its row sum in column 72) of the group's
+    // query tile, read from TMEM, scaled by 1 / row sum. F16 rows are staged as this
+    // warp's 32 x 72 block in the group's P buffer (free once the item's last P V has
+    // finished) and written by one TMA store that clips the rows past the image's last
+    // token; E4M3 rows are stored directly.
+    auto finish_item = [&](int n, int tl) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), tl & 1, abort_flag, p.err))) return false;
+      tc_fence_after();
+      const Item I = item_of(int(blockIdx.x) + n * int(gridDim.x), nq, p.H);
+      const int tq0 = (2 * I.qp + w) * kTile + sub * 32;  // first query row of this warp
+      const int tq = tq0 + lane;
+      uint8_t* stg = pbuf + sub * (32 * kDh * 2) + lane * (kDh * 2);
+      uint8_t* dst8 = static_cast<uint8_t*>(p.out) + (size_t(I.b) * size_t(T) + size_t(tq)) * size_t(D) + size_t(I.h) * kDh;
+      // columns 64..79 first: column 72 holds the row sum
+      uint32_t e[16];
+      tmem_ld16(o_tm + 64, e);
+      tmem_ld_wait();
+      asm volatile("" : "+r"(e[0]), "+r"(e[1]), "+r"(e[2]), "+r"(e[3]), "+r"(e[4]), "+r"(e[5]), "+r"(e[6]), "+r"(e[7]),
+                   "+r"(e[8]));
+      const float inv = 1.0f / __uint_as_float(e[8]);
+      auto emit8 = [&](const uint32_t* v, int g) {  // output columns 8 g .. 8 g + 7
+        if (!p.out_e4m3) {
+          uint4 wv;
+          __half2* hw = reinterpret_cast<__half2*>(&wv);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            hw[i] = __floats2half2_rn(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+          *reinterpret_cast<uint4*>(stg + 16 * g) = wv;
+        } else if (tq < T) {
+          uint2 wv;
+          __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&wv);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            q[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * __uint_as_float(v[2 * i]) * inv,
+                                                        16.0f * __uint_as_float(v[2 * i + 1]) * inv),
+                                            __NV_SATFINITE, __NV_E4M3);
+          *reinterpret_cast<uint2*>(dst8 + 8 * g) = wv;
+        }
+      };
+      emit8(e, 8);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[16];
+        tmem_ld16(o_tm + 16 * c, v);
+        tmem_ld_wait();
+        asm volatile("" : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                     "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+                     "+r"(v[14]), "+r"(v[15]));
+        emit8(v, 2 * c);
+        emit8(v + 8, 2 * c + 1);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kBarOEmpty + w));  // the next item's first P V may overwrite O
+      if (!p.out_e4m3) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && tq0 < T) {
+          tma_store_3d(&tm_out, smem_u32(pbuf + sub * (32 * kDh * 2)), I.h * kDh, tq0, I.b);
+          bulk_commit();
+        }
+      }
+      return true;
+    };
     // Reference maximum (log2 units) of this row's P tiles and of the O accumulator
     // in TMEM; the softmax denominator accumulates in O's column 72.
     float m = -INFINITY;
     bool ok = true;
+    int pend = -1;      // item whose output rows are still to be written (its last tile: pend_t)
+    int pend_t = 0;
+    int staged = 0;     // items whose output went through the staging rows
 
     for (int t = 0; t < total && ok; ++t) {
       const int n = t / nkv, j = t - n * nkv;
@@ -369,6 +442,21 @@ __global__ void __maxnreg__(168) attention_kernel(const Params p) {
       reg_fence(sv[3]);
       tc_fence_before();
       mbar_arrive(bar(kBarSEmpty + w));
+      // The previous item's output, now that its last P V has had time to finish.
+      bool wait_stage = false;
+      if (pend >= 0) {
+        if (!finish_item(pend, pend_t)) {
+          ok = false;
+          break;
+        }
+        pend = -1;
+        if (!p.out_e4m3) {
+          wait_stage = true;
+          if (lane == 0) bulk_wait_read<0>();  // this warp's store has read its staging rows
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarStage + w));
+        }
+      }
       const int valid = T - j * kTile;  // keys of this tile that exist (>= 1)
       if (valid < kTile) {              // keys past the last token: -inf, so P = 0 exactly
 #pragma unroll
@@ -377,16 +465,21 @@ __global__ void __maxnreg__(168) attention_kernel(const Params p) {
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= valid) sv[c][i] = 0xff800000u;
       }
-      // row maximum: four independent chains, then combined
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // row maximum: eight independent chains, then combined
+      float mq[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int k = 0; k < 8; ++k) mq[k] = fmaxf(__uint_as_float(sv[k >> 1][(k & 1) * 16]), __uint_as_float(sv[k >> 1][(k & 1) * 16 + 1]));
 #pragma unroll
-        for (int i = 0; i < 32; i += 8)
+      for (int k = 0; k < 8; ++k)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mq[k] = fmax3(mq[k], __uint_as_float(sv[c][i + 2 * k]), __uint_as_float(sv[c][i + 2 * k + 1]));
-      const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
+        for (int i = 2; i < 16; i += 2) {
+#ifdef EXP_MAXF
+          mq[k] = fmaxf(mq[k], fmaxf(__uint_as_float(sv[k >> 1][(k & 1) * 16 + i]), __uint_as_float(sv[k >> 1][(k & 1) * 16 + i + 1])));
+#else
+          mq[k] = fmax3(mq[k], __uint_as_float(sv[k >> 1][(k & 1) * 16 + i]), __uint_as_float(sv[k >> 1][(k & 1) * 16 + i + 1]));
+#endif
+        }
+      const float mx = fmaxf(fmaxf(fmax3(mq[0], mq[1], mq[2]), fmax3(mq[3], mq[4], mq[5])), fmaxf(mq[6], mq[7]));
       const float m_tile = mx * sl2;
       const bool raise = m_tile > m + kSlack;  // always on an item's first tile
       const float m_new = raise ? m_tile : m;
@@ -412,6 +505,12 @@ __global__ void __maxnreg__(168) attention_kernel(const Params p) {
         tmem_st_wait();
       }
       m = m_new;
+      // every warp of the group has finished reading the staging rows (they alias P)
+      if (wait_stage && !__all_sync(0xffffffffu, mbar_wait(bar(kBarStage + w), staged & 1, abort_flag, p.err))) {
+        ok = false;
+        break;
+      }
+      staged += wait_stage ? 1 : 0;
       // P = 2^(scale log2(e) s - m) as F16, in two halves of 64 keys; a half's buffer
       // is free once O += P V of the same half of the previous tile has finished
 #pragma unroll
@@ -442,58 +541,13 @@ __global__ void __maxnreg__(168) attention_kernel(const Params p) {
       }
       if (!ok) break;
 
-      if (j == nkv - 1) {  // the item's last tile: O / row sum -> output rows
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), t & 1, abort_flag, p.err))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t a[32], c[32], e[16];
-        tmem_ld32(o_tm, a);
-        tmem_ld32(o_tm + 32, c);
-        tmem_ld16(o_tm + 64, e);
-        tmem_ld_wait(a);
-        reg_fence(c);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(bar(kBarOEmpty + w));  // the next item's first P V may overwrite O
-        const Item I = item_of(int(blockIdx.x) + n * int(gridDim.x), nq, p.H);
-        const int tq = (2 * I.qp + w) * kTile + r;
-        if (tq < T) {
-          const float inv = 1.0f / __uint_as_float(e[8]);
-          const int D = p.H * kDh;
-          const size_t row = size_t(I.b) * size_t(T) + size_t(tq);
-          if (!p.out_e4m3) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + row * size_t(D) + size_t(I.h) * kDh);
-#pragma unroll
-            for (int g = 0; g < kGroups; ++g) {
-              const uint32_t* src = g < 4 ? a + 8 * g : (g < 8 ? c + 8 * (g - 4) : e);
-              uint4 wv;
-              __half2* hw = reinterpret_cast<__half2*>(&wv);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                hw[i] = __floats2half2_rn(__uint_as_float(src[2 * i]) * inv, __uint_as_float(src[2 * i + 1]) * inv);
-              dst[g] = wv;
-            }
-          } else {
-            uint2* dst =
-                reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * size_t(D) + size_t(I.h) * kDh);
-#pragma unroll
-            for (int g = 0; g < kGroups; ++g) {
-              const uint32_t* src = g < 4 ? a + 8 * g : (g < 8 ? c + 8 * (g - 4) : e);
-              uint2 wv;
-              __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&wv);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                q[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * __uint_as_float(src[2 * i]) * inv,
-                                                            16.0f * __uint_as_float(src[2 * i + 1]) * inv),
-                                                __NV_SATFINITE, __NV_E4M3);
-              dst[g] = wv;
-            }
-          }
-        }
+      if (j == nkv - 1) {  // the item's output is written during the next item's first tile
+        pend = n;
+        pend_t = t;
       }
     }
+    if (ok && pend >= 0) ok = finish_item(pend, pend_t);
+    if (lane == 0) bulk_wait_all();  // output stores have read shared memory before the CTA exits
     tmem_ld_wait();
   }
   __syncthreads();
@@ -520,12 +574,13 @@ __global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restric
 }
 
 // Buffer configuration: 0 = two Q buffers, 2 + 2 K / V stages; 1 = one Q buffer,
-// 3 + 3 stages; 2 = one Q buffer, 4 K + 2 V stages.
-int g_attention_config = 0;
+// 3 + 3 stages; 2 = one Q buffer, 4 K + 2 V stages. All three fill the same shared
+// memory; 1 measured fastest at 16 heads x 729 tokens (B = 32: 137 / 139 / 139 us).
+int g_attention_config = 1;
 int attention_config() { return g_attention_config; }
 
 template <int QB, int KS, int VS>
-sv_status attention_launch_cfg(const Params& p, int grid, cudaStream_t s) {
+sv_status attention_launch_cfg(const CUtensorMap& tmo, const Params& p, int grid, cudaStream_t s) {
   static bool attr_set = false;
   auto kern = attention_kernel<QB, KS, VS>;
   if (!attr_set) {
@@ -533,7 +588,7 @@ sv_status attention_launch_cfg(const Params& p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
     attr_set = true;
   }
-  kern<<<unsigned(grid), kThreads, Smem<QB, KS, VS>::kBytes, s>>>(p);
+  kern<<<unsigned(grid), kThreads, Smem<QB, KS, VS>::kBytes, s>>>(tmo, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return SV_OK;
@@ -568,10 +623,21 @@ sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, fl
   const int items = ((T + 2 * kTile - 1) / (2 * kTile)) * H * B;
   const int sms = num_sms() > 0 ? num_sms() : 1;
   const int grid = items < sms ? items : sms;
+  // F16 output rows are written by TMA stores of 32 x 72 blocks: [B][T][D] as a 3-D
+  // tensor, so a block's rows past an image's last token are clipped.
+  CUtensorMap tmo;
+  memset(&tmo, 0, sizeof(tmo));
+  if (!out_e4m3) {
+    const uint64_t dims[3] = {uint64_t(H) * kDh, uint64_t(T), uint64_t(B)};
+    const uint64_t strides[2] = {uint64_t(H) * kDh * 2, uint64_t(T) * H * kDh * 2};
+    const uint32_t box[3] = {uint32_t(kDh), 32, 1};
+    sv_status st = make_tmap(&tmo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, o, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != SV_OK) return st;
+  }
   switch (attention_config()) {
-    case 1: return attention_launch_cfg<1, 3, 3>(p, grid, s);
-    case 2: return attention_launch_cfg<1, 4, 2>(p, grid, s);
-    default: return attention_launch_cfg<2, 2, 2>(p, grid, s);
+    case 1: return attention_launch_cfg<1, 3, 3>(tmo, p, grid, s);
+    case 2: return attention_launch_cfg<1, 4, 2>(tmo, p, grid, s);
+    default: return attention_launch_cfg<2, 2, 2>(tmo, p, grid, s);
   }
 }
 
