@@ -49,15 +49,18 @@ struct Cfg {
   static constexpr int kStageA = kBM * kBKBytes;
   static constexpr int kStageB = (PAIR ? BN / 2 : BN) * kBKBytes;
   static constexpr int kStage = kStageA + kStageB;
-  // epilogue staging: per epilogue warp two 32 x 32 output blocks and two residual blocks
+  // epilogue staging: per epilogue warp a ring of four 32 x 32 blocks (residual in,
+  // result out)
   static constexpr int kEpiBlock = 2048;
-  static constexpr int kEpiBytes = 4 * 2 * kEpiBlock * 2;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kEpiRing = 4;
+  static constexpr int kEpiBytes = 4 * kEpiRing * kEpiBlock;
+  static constexpr int kBarBytes = 320;
   static constexpr int kBudget = 232448 - 1024 - kEpiBytes - kBarBytes;
   static constexpr int kStages = kBudget / kStage < 8 ? kBudget / kStage : 8;
   static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
   static constexpr int kSmem = 1024 + kStages * kStage + kEpiBytes + kBarBytes;
   static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
+  static_assert(8 * (2 * kStages + 5 + 4 * kEpiRing) + 8 <= kBarBytes, "barrier area");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + C::kStages * C::kStage;  // [4 warps][2] out blocks, then [4 warps][2] residual blocks
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::kEpiBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 13);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5 + 4 * C::kEpiRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_tfull = bar_empty + 8 * C::kStages;
   const uint32_t bar_tempty = bar_tfull + 16;
   const uint32_t bar_drain = bar_tempty + 16;
-  const uint32_t bar_res = bar_drain + 8;  // [4 warps][2]
+  const uint32_t bar_res = bar_drain + 8;  // [4 warps][ring]
 
   // Work items: tiles, or (PAIR) 256-row tiles shared by the two CTAs of a cluster.
   const int rank = PAIR ? int(cluster_ctarank()) : 0;
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_tempty + 8 * a, PAIR ? 256 : 128);  // every epilogue thread (of both CTAs) arrives
     }
     mbar_init(bar_drain, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(bar_res + 8 * i, 1);
+    for (int i = 0; i < 4 * C::kEpiRing; ++i) mbar_init(bar_res + 8 * i, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -324,31 +327,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (64-byte rows with the 64-byte swizzle for F16, 32-byte rows with the 32-byte
     // swizzle for E4M3) and written by one TMA store, which also clips the M / N tails.
     const int sub = warp & 3, ew = warp - 2;
-    uint8_t* obuf = epi + ew * 2 * C::kEpiBlock;
-    uint8_t* rbuf = epi + 4 * 2 * C::kEpiBlock + ew * 2 * C::kEpiBlock;
-    const uint32_t rbar = bar_res + 16 * ew;
-    // Residual loads in flight per buffer, with the phase parity that completes them.
-    bool res_issued[2] = {false, false};
-    uint32_t res_par[2] = {0, 0};
-    // Issues the residual load of chunk c of `tile` (the chunk with counter qq) into buffer qq & 1.
-    auto prefetch = [&](int mt, int nt, int c, int qq) {
-      const int b = qq & 1;
-      res_issued[b] = true;
-      res_par[b] = (qq >> 1) & 1;
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(rbar + 8 * b, C::kEpiBlock);
-        tma_load_2d(smem_u32(rbuf + b * C::kEpiBlock), &tmR, rbar + 8 * b, nt * BN + 32 * c, mt * kBM + sub * 32);
+    // Ring of kEpiRing blocks per warp; chunk q (counted over all of this warp's tiles)
+    // uses block q % kEpiRing. With a residual, the residual block of chunk q is
+    // loaded there two chunks ahead, the result overwrites it in place and the TMA
+    // store of the result reads it; the load of chunk q + 2 reuses the block of chunk
+    // q - 2 once that chunk's store has read it.
+    uint8_t* ring = epi + ew * C::kEpiRing * C::kEpiBlock;
+    const uint32_t rbar = bar_res + 8 * C::kEpiRing * ew;
+    // residual loads in flight per block, with the phase parity that completes them
+    uint32_t res_issued = 0, res_par = 0;
+    // prefetch cursor: next chunk whose residual is to be loaded (work item, chunk, counter)
+    int pit = it0, pc = 0, pq = 0;
+    auto prefetch_upto = [&](int qmax) {  // issue residual loads for chunks pq .. qmax
+      while (p.has_res && pq <= qmax && pit < num_items) {
+        int mt2, nt2;
+        tile_of<PAIR>(p, pit, rank, mt2, nt2);
+        const int kb = pq % C::kEpiRing;
+        res_issued |= 1u << kb;
+        res_par = (res_par & ~(1u << kb)) | ((uint32_t(pq / C::kEpiRing) & 1u) << kb);
+        if (lane == 0) {
+          bulk_wait_read<C::kEpiRing - 3>();  // the store that last read this block is done
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(rbar + 8 * kb, C::kEpiBlock);
+          tma_load_2d(smem_u32(ring + kb * C::kEpiBlock), &tmR, rbar + 8 * kb, nt2 * BN + 32 * pc,
+                      mt2 * kBM + sub * 32);
+        }
+        ++pq;
+        if (++pc >= tile_chunks(p, nt2, BN)) {
+          pc = 0;
+          pit += it_step;
+        }
       }
     };
-    // residual prefetch of chunk c of work item `it` (the chunk with counter qq)
-    auto prefetch_item = [&](int it, int c, int qq) {
-      int mt, nt;
-      tile_of<PAIR>(p, it, rank, mt, nt);
-      prefetch(mt, nt, c, qq);
-    };
-    if (p.has_res && it0 < num_items) prefetch_item(it0, 0, 0);
-    int q = 0;  // chunk counter of this warp: selects buffers and parities
+    prefetch_upto(1);
+    int q = 0;  // chunk counter of this warp: selects blocks and parities
     int local = 0;
     bool ok = true;
     const uint32_t tempty_lead0 = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
@@ -373,15 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_bias(p, n0, bq);
 #pragma unroll 1
       for (int c = 0; c < nch; ++c, ++q) {
-        const int b = q & 1;
-        if (p.has_res) {  // the next chunk's residual goes into the other buffer
-          int it2 = it, c2 = c + 1;
-          if (c2 >= nch) {
-            it2 = it + it_step;
-            c2 = 0;
-          }
-          if (it2 < num_items) prefetch_item(it2, c2, q + 1);
-        }
+        const int kb = q % C::kEpiRing;
+        uint8_t* blk = ring + kb * C::kEpiBlock;
+        prefetch_upto(q + 2);
         const int n = n0 + 32 * c;
         const int ngroups = min(4, (p.N - n) / 8);  // groups of 8 columns below N
         tmem_ld_wait(r);
@@ -416,16 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
         }
         if (p.has_res) {
-          if (!__all_sync(0xffffffffu, mbar_wait(rbar + 8 * b, (q >> 1) & 1, abort_flag, p.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(rbar + 8 * kb, uint32_t(q / C::kEpiRing) & 1u, abort_flag, p.err))) {
             ok = false;
             break;
           }
-          const uint8_t* rrow = rbuf + b * C::kEpiBlock + lane * 64;
+          const uint8_t* rrow = blk + lane * 64;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const uint4 u = *reinterpret_cast<const uint4*>(rrow + 16 * (g ^ ((lane >> 1) & 3)));
             add8h(u, v + 8 * g);
           }
+          __syncwarp();  // every lane has read its residual row before the block is overwritten
         }
         if (p.blk) {  // head-blocked layout for attention: 16-byte stores, consecutive rows contiguous
           if (row < p.M) {
@@ -451,10 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           continue;
         }
-        // the store issued two chunks ago from this buffer has finished reading it
-        if (lane == 0) bulk_wait_read<1>();
-        __syncwarp();
-        uint8_t* blk = obuf + b * C::kEpiBlock;
+        if (!p.has_res) {  // the store that last read this block (kEpiRing chunks ago) is done
+          if (lane == 0) bulk_wait_read<C::kEpiRing - 1>();
+          __syncwarp();
+        }
         if (!p.out_e4m3) {
           uint8_t* orow = blk + lane * 64;
 #pragma unroll
@@ -494,8 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_ld_wait();  // a load of the next chunk may be in flight after an abort
     if (lane == 0) {
       bulk_wait_all();  // every store has read shared memory and written global memory
-      for (int b = 0; b < 2; ++b)
-        if (res_issued[b]) mbar_wait_bounded(rbar + 8 * b, res_par[b], p.err);
+      for (int k = 0; k < C::kEpiRing; ++k)
+        if (res_issued & (1u << k)) mbar_wait_bounded(rbar + 8 * k, (res_par >> k) & 1u, p.err);
     }
     __syncwarp();
   }
