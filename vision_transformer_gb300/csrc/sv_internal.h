@@ -50,6 +50,9 @@ struct GemmEpi {
 // The operand side of a GEMM: tensor maps for A and W plus the sizes.
 struct GemmOperands {
   CUtensorMap ta, tw, tc, tr;  // A, W, output, residual
+  CUtensorMap tw_tail;         // W rows of the narrow last column tile (CTA pairs)
+  int tail_n = 0;              // MMA N of the narrow last column tile, 0 if all tiles are full
+  int tail_last = 0;           // narrow tiles after all full ones in the work order
   int M = 0, N = 0, K = 0;
   int fp8 = 0;
   int bn = 0;
