@@ -240,9 +240,6 @@ def main():
         dist.barrier()
     torch.cuda.synchronize(dev)
     vt.sv_launch_count()
-    vt.sv_profile_enable(True)
-    for k in range(vt.KIND_OTHER + 1):
-        vt.sv_profile_read(k)  # drop warm-up records
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         e0.record(stream)
@@ -252,11 +249,25 @@ def main():
         torch.cuda.synchronize(dev)
     vt.sv_sync(stream)
     launches = vt.sv_launch_count()
-    vt.sv_profile_enable(False)
-    prof = {vt.KIND_NAMES[k]: vt.sv_profile_read(k) for k in range(vt.KIND_OTHER + 1)}
     elapsed_ms = max_over_ranks(e0.elapsed_time(e1), world)
     ms_per_step = elapsed_ms / args.steps
     value = B * world / (ms_per_step / 1e3)
+
+    # ---- per-kernel times: the same steps again, every library launch bracketed by
+    # CUDA events on its stream (the brackets add small gaps, so this second timed region
+    # gives the kernel durations and shares, not the step time above)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    vt.sv_profile_enable(True)
+    for k in range(vt.KIND_OTHER + 1):
+        vt.sv_profile_read(k)  # drop earlier records
+    for _ in range(args.steps):
+        step()
+    vt.sv_sync(stream)
+    vt.sv_profile_enable(False)
+    prof = {vt.KIND_NAMES[k]: vt.sv_profile_read(k) for k in range(vt.KIND_OTHER + 1)}
 
     # ---- end to end: pinned host pixels in, host embedding out, every step
     host_pix = pix.cpu().pin_memory()
