@@ -139,6 +139,24 @@ sv_status sv_layernorm(const void* x, const void* gamma, const void* beta, void*
                        int out_dtype, void* stream);
 
 /*
+ * C[M,N] = act(LayerNorm(x)[M,K] . W[N,K]^T + bias[N]), F16 in and out: a
+ * pre-normalised projection ("SigLIP ViT benchmark": the LN1 -> QKV and
+ * LN2 -> MLP-up pairs of each layer) with the LayerNorm folded into the GEMM
+ * instead of written out: the row mean and 1/sqrt(var + eps) (F32, centred
+ * variance) come from a statistics pass over x, W is scaled by gamma, and the
+ * epilogue applies r (x . W' - mean * colsum(W')) + bias + W . beta in F32 before
+ * the activation. This is what sv_encode runs in F16 mode.
+ * x: f16 [M, K]; gamma, beta: f16 [K]; W: f16 [N, K] (K-major); bias: f16 [N]
+ * or NULL; C: f16 [M, N]; act: sv_act.
+ * Requirements: M >= 1; N, K multiples of 16; K <= 4096; pointers 16-byte
+ * aligned. The call keeps a scratch buffer (scaled weights and statistics) that
+ * grows to the largest call and is freed by sv_shutdown.
+ * Errors: SV_ERR_INVALID_ARG, SV_ERR_OOM, SV_ERR_CUDA.
+ */
+sv_status sv_ln_gemm(const void* x, const void* gamma, const void* beta, float eps, const void* W, const void* bias,
+                     void* C, int M, int N, int K, int act, void* stream);
+
+/*
  * Multi-head self-attention with F32 softmax and accumulation ("SigLIP ViT
  * benchmark", precision paragraph; padding is never read as data: "SigLIP
  * optimized execution and PV padding", cause and fix).

@@ -66,6 +66,9 @@ def test_errors_before_device_work(lib):
         vt.SV_ERR_INVALID_ARG
     assert lib.sv_gemm_bias_act(p16, p16, None, None, 1, None, p16, 16, 16, 16, 0, 3, 0, 1.0, None) == \
         vt.SV_ERR_INVALID_ARG
+    # LayerNorm folded into a GEMM: K beyond the LayerNorm's 4096, or N not a multiple of 16
+    assert lib.sv_ln_gemm(p16, p16, p16, 1e-6, p16, None, p16, 16, 16, 8192, 0, None) == vt.SV_ERR_INVALID_ARG
+    assert lib.sv_ln_gemm(p16, p16, p16, 1e-6, p16, None, p16, 16, 24, 16, 0, None) == vt.SV_ERR_INVALID_ARG
     # LayerNorm width must be a multiple of 8 (even, unpadded rows: LayerNorm paragraph)
     assert lib.sv_layernorm(p16, p16, p16, p16, 4, 12, 1e-6, 0, None) == vt.SV_ERR_INVALID_ARG
     # head width other than 72 is not implemented

@@ -137,6 +137,30 @@ def test_layernorm(sv, rows, width):
     assert_close(decode_e4m3(y8).reshape(rows, width), ref, 2.0 ** -3 + RT, 2.0 ** -10, "layernorm e4m3")
 
 
+@pytest.mark.parametrize("M,N,K,act", [(729, 3456, 1152, 0), (777, 4304, 1152, 1), (200, 48, 80, 0)])
+def test_ln_gemm_folded(sv, M, N, K, act):
+    """LayerNorm folded into the following GEMM (the encoder's F16 LN1->QKV and
+    LN2->MLP-up pairs) against the oracle's LayerNorm followed by its linear map.
+    Rows with a large mean (x*3 + 1.5) exercise the mean correction; the folded
+    path keeps LN(x) in F32 where the unfolded one rounds it to F16, and rounds
+    W*gamma to F16 instead, so the tolerance is two F16 roundings of the output scale."""
+    x = (synth.normal(71, 1, (M, K)).astype(np.float32) * 3 + 1.5).astype(np.float16)
+    g = synth.normal(71, 2, (K,), mean=1.0, std=0.2)
+    bt = synth.normal(71, 3, (K,), std=0.2)
+    W = synth.normal(71, 4, (K, N), std=1.0 / np.sqrt(K))
+    b = synth.normal(71, 5, (N,), std=0.01)
+    C = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    sv.sv_ln_gemm(dev_f16(x), dev_f16(g), dev_f16(bt), dev_f16(W.T), dev_f16(b), C, M, N, K, act=act)
+    sv.sv_sync()
+    ref = oracle.linear(oracle.layernorm(x, g, bt), W, b, act=act)
+    assert_close(host(C), ref, RT, 2 * RT * _scale(ref), f"ln_gemm {M}x{N}x{K}")
+    # the weights passed in are left unchanged (the call scales a private copy)
+    C2 = torch.empty_like(C)
+    sv.sv_ln_gemm(dev_f16(x), dev_f16(g), dev_f16(bt), dev_f16(W.T), dev_f16(b), C2, M, N, K, act=act)
+    sv.sv_sync()
+    assert torch.equal(C, C2)
+
+
 def _attn_ref(qkv, H):
     D = H * 72
     return oracle.attention(qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:], H, 72)
@@ -227,6 +251,9 @@ def test_bounded_wait_reports_timeout_and_context_survives(sv):
 
 def test_gpu_argument_errors(sv):
     x = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(sv.SvError) as e:
+        sv.sv_ln_gemm(x, x, x, x, None, x, 64, 64, 8000)
+    assert e.value.status == sv.SV_ERR_INVALID_ARG
     with pytest.raises(sv.SvError) as e:
         sv.sv_gemm_bias_act(x, x, None, None, 1, None, x, 64, 60, 64)
     assert e.value.status == sv.SV_ERR_INVALID_ARG

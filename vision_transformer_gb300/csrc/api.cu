@@ -75,12 +75,16 @@ struct Dims {
 struct LayerW {
   __half *ln1_g, *ln1_b, *qkv_w, *qkv_b, *out_w, *out_b, *ln2_g, *ln2_b, *fc1_w, *fc1_b, *fc2_w, *fc2_b;
   uint8_t *qkv_w8, *out_w8, *fc1_w8, *fc2_w8;
+  // LayerNorms folded into the F16 QKV and MLP-up GEMMs: qkv_w / fc1_w hold W * gamma
+  // (the E4M3 copies keep W); the GEMMs' extra K block rows [N, 16] and combined biases
+  __half *qkv_aug, *qkv_bf, *fc1_aug, *fc1_bf;
 };
 
 struct Weights {
   bool ready = false;
   Dims d;
   void* arena = nullptr;
+  void* fold = nullptr;  // extra K block rows and combined biases of the folded LayerNorms
   __half *patch_w = nullptr, *patch_b = nullptr, *pos = nullptr;
   uint8_t* patch_w8 = nullptr;
   std::vector<LayerW> layers;
@@ -113,11 +117,14 @@ struct MapPlan {
 // Workspace and operand maps of the whole forward pass for one batch size and dtype.
 struct Plan {
   int B = 0, fp8 = 0;
+  bool fold_ln = false;  // LN1 / LN2 folded into the QKV / MLP-up GEMMs (F16 operands)
   void* mem = nullptr;
   size_t bytes = 0;
   void* A0 = nullptr;     // [M, Kp] staged pixels
   __half* X = nullptr;    // [M, D] residual stream
-  void* Y = nullptr;      // [M, D] LayerNorm output (GEMM operand)
+  void* Y = nullptr;       // [M, D] LayerNorm output (GEMM operand)
+  float* ln_r = nullptr;    // [M] 1/std of each row (F16 path: LayerNorm folded into the GEMMs)
+  __half* ln_aug = nullptr;  // [M, 16] the folded GEMMs' extra K block (-mean)
   __half* QKV = nullptr;  // head-blocked Q/K/V for attention; the MAP KV projection reuses it row-major
   void* O = nullptr;      // [M, D] attention output (GEMM operand)
   void* Hh = nullptr;     // [M, F] GELU output (GEMM operand)
@@ -129,6 +136,8 @@ std::map<std::pair<int, int>, std::unique_ptr<Plan>> g_plans;      // sv_encode
 std::map<std::pair<int, int>, std::unique_ptr<Plan>> g_map_plans;  // sv_map_pool
 void* g_attn_scratch = nullptr;  // head-blocked copy of sv_attention's input
 size_t g_attn_scratch_bytes = 0;
+void* g_lng_scratch = nullptr;  // sv_ln_gemm: scaled weights, column sums, biases, row statistics
+size_t g_lng_scratch_bytes = 0;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -140,11 +149,15 @@ void free_plans() {
   if (g_attn_scratch) cudaFree(g_attn_scratch);
   g_attn_scratch = nullptr;
   g_attn_scratch_bytes = 0;
+  if (g_lng_scratch) cudaFree(g_lng_scratch);
+  g_lng_scratch = nullptr;
+  g_lng_scratch_bytes = 0;
 }
 
 void free_weights() {
   free_plans();
   if (g_w.arena) cudaFree(g_w.arena);
+  if (g_w.fold) cudaFree(g_w.fold);
   g_w = Weights();
 }
 
@@ -262,6 +275,30 @@ sv_status init_weights(uint64_t seed, const Dims& d) {
       else if (name == "map_fc2_b") g_w.mfc2_b = p16;
     }
   }
+  // Fold LN1 into the QKV weights and LN2 into the MLP-up weights (F16 path); the
+  // E4M3 copies were quantised from the unscaled weights above.
+  {
+    const size_t per_layer = size_t(3 * d.D + d.F) * 17;  // halves: [N, 16] rows + [N] biases
+    void* fold = nullptr;
+    e = cudaMalloc(&fold, per_layer * size_t(d.L) * sizeof(__half));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      set_error("cudaMalloc for the folded LayerNorm constants failed: %s", cudaGetErrorString(e));
+      return SV_ERR_OOM;
+    }
+    g_w.fold = fold;
+    __half* f = static_cast<__half*>(fold);
+    for (int l = 0; l < d.L; ++l) {
+      LayerW& w = g_w.layers[size_t(l)];
+      w.qkv_aug = f;
+      w.fc1_aug = f + size_t(3 * d.D) * 16;
+      w.qkv_bf = f + size_t(3 * d.D + d.F) * 16;
+      w.fc1_bf = w.qkv_bf + 3 * d.D;
+      f += per_layer;
+      SV_TRY(fold_ln_launch(w.qkv_w, w.ln1_g, w.ln1_b, w.qkv_b, w.qkv_aug, w.qkv_bf, 3 * d.D, d.D, nullptr));
+      SV_TRY(fold_ln_launch(w.fc1_w, w.ln2_g, w.ln2_b, w.fc1_b, w.fc1_aug, w.fc1_bf, d.F, d.D, nullptr));
+    }
+  }
   SV_CHECK_CUDA(cudaDeviceSynchronize(), "weight initialisation");
   g_w.ready = true;
   return SV_OK;
@@ -284,7 +321,7 @@ sv_status make_call(GemmCall* c, const void* A, const void* W, int M, int N, int
                     int k_logical) {
   c->e = e;
   c->k = k_logical;
-  SV_TRY(gemm_prepare(&c->g, A, W, M, N, K, fp8));
+  SV_TRY(gemm_prepare(&c->g, A, W, M, N, K, fp8, e.ln_r == nullptr));
   return gemm_bind_epilogue(&c->g, c->e);
 }
 
@@ -353,11 +390,14 @@ sv_status get_plan(int B, int fp8, Plan** out) {
   std::unique_ptr<Plan> p(new Plan());
   p->B = B;
   p->fp8 = fp8;
+  p->fold_ln = !fp8;
   Carver c{nullptr};
   for (int pass = 0; pass < 2; ++pass) {
     p->A0 = c.take(M * d.Kp * eb);
     p->X = static_cast<__half*>(c.take(M * d.D * 2));
     p->Y = c.take(M * d.D * eb);
+    p->ln_r = static_cast<float*>(c.take(M * sizeof(float)));
+    p->ln_aug = static_cast<__half*>(c.take(M * 16 * sizeof(__half)));
     const size_t qkv_bytes = attention_blocked_bytes(B, d.T, d.H);
     p->QKV = static_cast<__half*>(c.take(qkv_bytes > M * 3 * d.D * 2 ? qkv_bytes : M * 3 * d.D * 2));
     p->O = c.take(M * d.D * eb);
@@ -387,16 +427,25 @@ sv_status get_plan(int B, int fp8, Plan** out) {
   for (int l = 0; l < d.L; ++l) {
     const LayerW& w = g_w.layers[size_t(l)];
     const size_t i = size_t(l);
-    GemmEpi qe = epi(w.qkv_b, p->QKV, sc);
+    // F16: LN1 / LN2 folded into the QKV / MLP-up GEMMs, which read X itself; E4M3:
+    // the LayerNorm kernels write the quantised operand Y
+    GemmEpi qe = epi(p->fold_ln ? w.qkv_bf : w.qkv_b, p->QKV, sc);
+    GemmEpi fe = epi(p->fold_ln ? w.fc1_bf : w.fc1_b, p->Hh, sc, SV_ACT_GELU_TANH, fp8);
+    if (p->fold_ln) {
+      qe.ln_r = fe.ln_r = p->ln_r;
+      qe.ln_aug_a = fe.ln_aug_a = p->ln_aug;
+      qe.ln_aug_w = w.qkv_aug;
+      fe.ln_aug_w = w.fc1_aug;
+    }
     qe.blk_out = p->QKV;
     qe.blk_T = d.T;
     qe.blk_H = d.H;
     qe.blk_B = B;
-    if ((st = make_call(&p->qkv[i], p->Y, fp8 ? (const void*)w.qkv_w8 : w.qkv_w, Mi, 3 * d.D, d.D, fp8, qe, d.D)) ||
+    const void* ln_in = p->fold_ln ? static_cast<const void*>(p->X) : p->Y;
+    if ((st = make_call(&p->qkv[i], ln_in, fp8 ? (const void*)w.qkv_w8 : w.qkv_w, Mi, 3 * d.D, d.D, fp8, qe, d.D)) ||
         (st = make_call(&p->out[i], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8,
                         epi(w.out_b, p->X, sc, SV_ACT_NONE, 0, p->X), d.D)) ||
-        (st = make_call(&p->fc1[i], p->Y, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8,
-                        epi(w.fc1_b, p->Hh, sc, SV_ACT_GELU_TANH, fp8), d.D)) ||
+        (st = make_call(&p->fc1[i], ln_in, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8, fe, d.D)) ||
         (st = make_call(&p->fc2[i], p->Hh, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, Mi, d.D, d.F, fp8,
                         epi(w.fc2_b, p->X, sc, SV_ACT_NONE, 0, p->X), d.F)))
       return fail(st);
@@ -418,6 +467,12 @@ double gemm_bytes(const GemmOperands& g, const GemmEpi& e, int k_logical) {
 sv_status run_gemm(const GemmCall& c, cudaStream_t s) {
   Launch L(kKindGemm, gemm_flops(c.g, c.k), gemm_bytes(c.g, c.e, c.k), s);
   return gemm_launch(c.g, c.e, s);
+}
+
+sv_status run_ln_stats(const __half* x, float* r, __half* aug, int rows, cudaStream_t s) {
+  const int D = g_w.d.D;
+  Launch L(kKindLN, 4.0 * rows * D, double(rows) * (D * 2.0 + 36.0), s);
+  return ln_stats_launch(x, r, aug, rows, D, 1e-6f, s);
 }
 
 sv_status run_ln(const __half* x, const __half* gm, const __half* bt, void* y, int rows, int out_e4m3,
@@ -460,7 +515,7 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
   for (int l = 0; l < layers; ++l) {
     const LayerW& w = g_w.layers[size_t(l)];
     const size_t i = size_t(l);
-    SV_TRY(run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
+    SV_TRY(p.fold_ln ? run_ln_stats(p.X, p.ln_r, p.ln_aug, M, s) : run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
     SV_TRY(run_gemm(p.qkv[i], s));
     {
       Launch L(kKindAttn, 4.0 * B * d.H * double(d.T) * double(d.T) * 72.0,
@@ -468,7 +523,7 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
       SV_TRY(attention_launch(p.QKV, p.O, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, s));
     }
     SV_TRY(run_gemm(p.out[i], s));
-    SV_TRY(run_ln(p.X, w.ln2_g, w.ln2_b, p.Y, M, fp8, s));
+    SV_TRY(p.fold_ln ? run_ln_stats(p.X, p.ln_r, p.ln_aug, M, s) : run_ln(p.X, w.ln2_g, w.ln2_b, p.Y, M, fp8, s));
     SV_TRY(run_gemm(p.fc1[i], s));
     SV_TRY(run_gemm(p.fc2[i], s));
   }
@@ -646,6 +701,65 @@ sv_status sv_gemm_bias_act(const void* A, const void* W, const void* bias, const
   GemmCall c;
   SV_TRY(make_call(&c, A, W, M, N, K, in_dtype, e, K));
   return run_gemm(c, static_cast<cudaStream_t>(stream));
+}
+
+sv_status sv_ln_gemm(const void* x, const void* gamma, const void* beta, float eps, const void* W, const void* bias,
+                     void* C, int M, int N, int K, int act, void* stream) {
+  if (!x || !gamma || !beta || !W || !C || M < 1 || N < 16 || N % 16 || K < 16 || K % 16 || K > 4096 ||
+      !(eps >= 0.0f) || (act != 0 && act != 1)) {
+    set_error("sv_ln_gemm: bad arguments (M %d N %d K %d; N, K multiples of 16, K <= 4096)", M, N, K);
+    return SV_ERR_INVALID_ARG;
+  }
+  if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(beta, 16) || !aligned(W, 16) || !aligned(bias, 16) ||
+      !aligned(C, 16)) {
+    set_error("sv_ln_gemm: pointers must be 16-byte aligned");
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_TRY(ensure_runtime());
+  // scratch: W * gamma [N, K] | W's extra K block [N, 16] | biases [N] | x's extra K block
+  // [M, 16] (all f16) | 1/std [M] f32
+  const size_t off_wa = align_up(size_t(N) * K * 2, 256), off_b = align_up(off_wa + size_t(N) * 32, 256),
+               off_xa = align_up(off_b + size_t(N) * 2, 256), off_r = align_up(off_xa + size_t(M) * 32, 256),
+               need = off_r + size_t(M) * 4;
+  if (need > g_lng_scratch_bytes) {  // grows monotonically; freed by sv_shutdown
+    if (g_lng_scratch) {
+      SV_CHECK_CUDA(cudaDeviceSynchronize(), "sv_ln_gemm");
+      cudaFree(g_lng_scratch);
+      g_lng_scratch = nullptr;
+      g_lng_scratch_bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&g_lng_scratch, need);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      set_error("sv_ln_gemm: cudaMalloc of %zu bytes failed", need);
+      return SV_ERR_OOM;
+    }
+    g_lng_scratch_bytes = need;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* sc = static_cast<char*>(g_lng_scratch);
+  __half* w2 = reinterpret_cast<__half*>(sc);
+  __half* wa = reinterpret_cast<__half*>(sc + off_wa);
+  __half* bf = reinterpret_cast<__half*>(sc + off_b);
+  __half* xa = reinterpret_cast<__half*>(sc + off_xa);
+  float* rr = reinterpret_cast<float*>(sc + off_r);
+  SV_CHECK_CUDA(cudaMemcpyAsync(w2, W, size_t(N) * K * 2, cudaMemcpyDeviceToDevice, s), "sv_ln_gemm weight copy");
+  {
+    Launch L(kKindOther, 0.0, double(N) * K * 4.0, s);
+    SV_TRY(fold_ln_launch(w2, static_cast<const __half*>(gamma), static_cast<const __half*>(beta),
+                          static_cast<const __half*>(bias), wa, bf, N, K, s));
+  }
+  {
+    Launch L(kKindLN, 4.0 * M * K, double(M) * (K * 2.0 + 8.0), s);
+    SV_TRY(ln_stats_launch(static_cast<const __half*>(x), rr, xa, M, K, eps, s));
+  }
+  GemmEpi e = epi(bf, C, 1.0f, act);
+  e.ln_r = rr;
+  e.ln_aug_a = xa;
+  e.ln_aug_w = wa;
+  GemmCall c;
+  SV_TRY(make_call(&c, x, w2, M, N, K, 0, e, K));
+  return run_gemm(c, s);
 }
 
 sv_status sv_layernorm(const void* x, const void* gamma, const void* beta, void* y, int rows, int width, float eps,

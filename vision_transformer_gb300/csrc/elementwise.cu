@@ -28,11 +28,15 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 // LayerNorm, one warp per row ("SigLIP ViT benchmark", LayerNorm paragraph):
 // mean, then the centred (biased) variance, both in F32 from the row held in
 // registers, then the affine map. Each lane owns CPL chunks of 4 values
-// (8-byte loads); a 1152-wide row is 9 chunks per lane.
+// (8-byte loads); a 1152-wide row is 9 chunks per lane. With `stats_r` set only
+// the row statistics are written: 1/sqrt(var + eps) to stats_r and, for the
+// consuming GEMM's extra K block, the F16 row (-mean_hi, -mean_hi, -mean_lo, 0...)
+// to stats_aug (mean_hi + mean_lo = mean to about 2^-22 relative).
 template <int CPL>
 __global__ void __launch_bounds__(256) layernorm_kernel(const __half* __restrict__ x, const __half* __restrict__ g,
                                                         const __half* __restrict__ bta, void* __restrict__ y,
-                                                        int rows, int width, float eps, int out_e4m3) {
+                                                        int rows, int width, float eps, int out_e4m3,
+                                                        float* __restrict__ stats_r, __half* __restrict__ stats_aug) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long row = long(blockIdx.x) * 8 + warp;
   if (row >= rows) return;
@@ -69,6 +73,21 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const __half* __restrict
     }
   const float var = warp_sum(q) / float(width);
   const float rstd = rsqrtf(var + eps);
+  if (stats_r) {  // statistics only: the normalisation is folded into the consuming GEMM
+    if (lane < 2) {  // row of the GEMM's extra K block: (-mean_hi, -mean_hi, -mean_lo, 0, ...)
+      const __half hi = __float2half_rn(-mean);
+      const __half lo = __float2half_rn(-mean - __half2float(hi));
+      const __half2 z = __float2half2_rn(0.0f);
+      uint4 u;  // lane 0: columns 0..7, lane 1: columns 8..15
+      __half2* h = reinterpret_cast<__half2*>(&u);
+      h[0] = lane == 0 ? __halves2half2(hi, hi) : z;
+      h[1] = lane == 0 ? __halves2half2(lo, __float2half_rn(0.0f)) : z;
+      h[2] = h[3] = z;
+      *reinterpret_cast<uint4*>(stats_aug + row * 16 + 8 * lane) = u;
+    }
+    if (lane == 0) stats_r[row] = rstd;
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
     const int c = lane + 32 * i;
@@ -233,29 +252,87 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, int* err) {
   }
 }
 
+// LayerNorm folded into the linear map that consumes it: with y = (x - mu) r . g + be
+// (r = 1/sqrt(var + eps)), y . W_n + b_n = r (x . W'_n - mu s_n) + b'_n where
+// W'_nk = g_k W_nk (rounded to F16, in place), s_n = sum_k W'_nk and
+// b'_n = b_n + sum_k be_k W_nk (stored in F16). The GEMM subtracts mu s_n as one
+// extra K block: this row of it is (s_hi, s_lo, s_hi, 0, ...) against the LayerNorm
+// input's (-mu_hi, -mu_hi, -mu_lo, 0, ...), so the tensor core adds -mu s exactly up
+// to the dropped mu_lo s_lo term. One warp per output row n; sums in F32.
+__global__ void __launch_bounds__(256) fold_ln_kernel(__half* __restrict__ W, const __half* __restrict__ g,
+                                                      const __half* __restrict__ be, const __half* __restrict__ b,
+                                                      __half* __restrict__ w_aug, __half* __restrict__ b_out, int N,
+                                                      int K) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long n = long(blockIdx.x) * 8 + warp;
+  if (n >= N) return;
+  __half* wr = W + n * long(K);
+  float s = 0.0f, t = 0.0f;
+  for (int k = lane; k < K; k += 32) {
+    const float w = __half2float(wr[k]);
+    t = fmaf(__half2float(be[k]), w, t);
+    const __half wg = __float2half_rn(w * __half2float(g[k]));
+    wr[k] = wg;
+    s += __half2float(wg);
+  }
+  s = warp_sum(s);
+  t = warp_sum(t);
+  if (lane < 2) {  // row of the extra K block: (s_hi, s_lo, s_hi, 0, ...)
+    const __half hi = __float2half_rn(s);
+    const __half lo = __float2half_rn(s - __half2float(hi));
+    const __half2 z = __float2half2_rn(0.0f);
+    uint4 u;
+    __half2* h = reinterpret_cast<__half2*>(&u);
+    h[0] = lane == 0 ? __halves2half2(hi, lo) : z;
+    h[1] = lane == 0 ? __halves2half2(hi, __float2half_rn(0.0f)) : z;
+    h[2] = h[3] = z;
+    *reinterpret_cast<uint4*>(w_aug + n * 16 + 8 * lane) = u;
+  }
+  if (lane == 0) b_out[n] = __float2half_rn((b ? __half2float(b[n]) : 0.0f) + t);
+}
+
 template <int CPL>
 void ln_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width, float eps,
-               int out_e4m3, cudaStream_t s) {
-  layernorm_kernel<CPL><<<(rows + 7) / 8, 256, 0, s>>>(x, g, b, y, rows, width, eps, out_e4m3);
+               int out_e4m3, float* stats_r, __half* stats_aug, cudaStream_t s) {
+  layernorm_kernel<CPL><<<(rows + 7) / 8, 256, 0, s>>>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug);
 }
 
 }  // namespace
 
-sv_status layernorm_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width,
-                           float eps, int out_e4m3, cudaStream_t s) {
+namespace {
+sv_status ln_any(const __half* x, const __half* g, const __half* b, void* y, int rows, int width, float eps,
+                 int out_e4m3, float* stats_r, __half* stats_aug, cudaStream_t s) {
   const int cpl = (width / 4 + 31) / 32;
-  if (cpl <= 1) ln_launch<1>(x, g, b, y, rows, width, eps, out_e4m3, s);
-  else if (cpl <= 2) ln_launch<2>(x, g, b, y, rows, width, eps, out_e4m3, s);
-  else if (cpl <= 4) ln_launch<4>(x, g, b, y, rows, width, eps, out_e4m3, s);
-  else if (cpl <= 9) ln_launch<9>(x, g, b, y, rows, width, eps, out_e4m3, s);
-  else if (cpl <= 16) ln_launch<16>(x, g, b, y, rows, width, eps, out_e4m3, s);
-  else if (cpl <= 32) ln_launch<32>(x, g, b, y, rows, width, eps, out_e4m3, s);
+  if (cpl <= 1) ln_launch<1>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 2) ln_launch<2>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 4) ln_launch<4>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 9) ln_launch<9>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 16) ln_launch<16>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 32) ln_launch<32>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
   else {
     set_error("layernorm: width %d too large", width);
     return SV_ERR_UNSUPPORTED;
   }
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "layernorm launch");
+}
+}  // namespace
+
+sv_status layernorm_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width,
+                           float eps, int out_e4m3, cudaStream_t s) {
+  return ln_any(x, g, b, y, rows, width, eps, out_e4m3, nullptr, nullptr, s);
+}
+
+sv_status ln_stats_launch(const __half* x, float* stats_r, __half* stats_aug, int rows, int width, float eps,
+                          cudaStream_t s) {
+  return ln_any(x, nullptr, nullptr, nullptr, rows, width, eps, 0, stats_r, stats_aug, s);
+}
+
+sv_status fold_ln_launch(__half* W, const __half* g, const __half* be, const __half* b, __half* w_aug, __half* b_out,
+                         int N, int K, cudaStream_t s) {
+  fold_ln_kernel<<<unsigned((N + 7) / 8), 256, 0, s>>>(W, g, be, b, w_aug, b_out, N, K);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "fold_ln launch");
 }
 
 sv_status pad_pixels_launch(const __half* pix, void* out, long rows, int P, int Kp, int out_e4m3, cudaStream_t s) {

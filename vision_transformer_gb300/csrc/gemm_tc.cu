@@ -76,6 +76,9 @@ struct Params {
   int has_res;
   int act, out_e4m3;
   float scale;
+  // LayerNorm folded in (see GemmEpi): 1/std per row, and one extra K block of 16
+  const float* ln_r;
+  int ln_aug;
   int* err;
   // head-blocked output (fused QKV projection feeding attention), or null
   uint8_t* blk;
@@ -156,7 +159,8 @@ template <int BN, bool FP8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmWt, const __grid_constant__ CUtensorMap tmC,
-                   const __grid_constant__ CUtensorMap tmR, const Params p) {
+                   const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmAa,
+                   const __grid_constant__ CUtensorMap tmWa, const Params p) {
   using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -174,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_res = bar_drain + 8;  // [4 warps][ring]
 
   // Work items: tiles, or (PAIR) 256-row tiles shared by the two CTAs of a cluster.
+  const int aug_blocks = (!PAIR && !FP8 && p.ln_aug) ? 1 : 0;  // folded LayerNorm's extra K block
   const int rank = PAIR ? int(cluster_ctarank()) : 0;
   const bool leader = rank == 0;
   const int it0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = it0; it < num_items && ok; it += it_step) {
         int mt, nt;
         tile_of<PAIR>(p, it, rank, mt, nt);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < p.k_blocks + aug_blocks; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.err)) {
             ok = false;
             break;
@@ -232,7 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = bar_full + 8 * stage;
           const uint32_t sa = smem_u32(smem + stage * C::kStage);
           const int kc = kb * (FP8 ? 128 : 64);
-          if (PAIR) {  // both CTAs' copies complete on the leader's barrier
+          if (kb == p.k_blocks) {  // folded LayerNorm: the 16-wide K block (-mean | column sums)
+            mbar_arrive_expect_tx(fb, (kBM + BN) * 32);
+            tma_load_2d(sa, &tmAa, fb, 0, mt * kBM);
+            tma_load_2d(sa + C::kStageA, &tmWa, fb, 0, nt * BN);
+          } else if (PAIR) {  // both CTAs' copies complete on the leader's barrier
             const uint32_t fb_lead = mapa_shared(fb, 0);
             if (nt == p.n_full && p.tail_n) {  // narrow tile: each CTA holds tail_n / 2 W rows
               if (leader) mbar_arrive_expect_tx(fb, 2 * (C::kStageA + (p.tail_n / 2) * kBKBytes));
@@ -290,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(acc * BN);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < p.k_blocks + aug_blocks; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err)) {
             ok = false;
             break;
@@ -298,6 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::kStage);
           const uint32_t sb = sa + C::kStageA;
+          if (!PAIR && !FP8 && kb == p.k_blocks) {
+            // 32-byte rows with the 32-byte swizzle: 8-row groups 256 bytes apart
+            mma_f16(d, make_sdesc(sa, 16, 256, 6), make_sdesc(sb, 16, 256, 6), idesc, 1u);
+          } else
 #pragma unroll
           for (int j = 0; j < 4; ++j) {  // 4 instructions x 32 bytes of K
             const uint64_t ad = make_sdesc(sa + 32 * j, 16, 1024, 2);
@@ -395,13 +408,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_of<PAIR>(p, it, rank, mt, nt);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      // every lane waits; the outcome is made warp-uniform so warp-collective steps stay converged
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.err))) break;
-      tc_fence_after();
       const int row0 = mt * kBM + sub * 32;
       const int row = row0 + lane;
       const int n0 = nt * BN;
       const int nch = tile_chunks(p, nt, BN);
+      // folded LayerNorm: 1/std of this row (requested before the accumulator wait, so
+      // its latency hides behind it) joins the dequantisation scale
+      const float row_scale = p.ln_r ? p.scale * __ldg(p.ln_r + (row < p.M ? row : p.M - 1)) : p.scale;
+      // every lane waits; the outcome is made warp-uniform so warp-collective steps stay converged
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.err))) break;
+      tc_fence_after();
       const uint32_t tbase = tmem_base + uint32_t(acc * BN) + (uint32_t(sub * 32) << 16);
       // The TMEM load and the bias of chunk c + 1 are issued as soon as chunk c's
       // accumulators are in registers, so their latency hides behind chunk c's math.
@@ -424,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 t = __half22float2(h[i]);
-            v[8 * g + 2 * i] = fmaf(__uint_as_float(r[8 * g + 2 * i]), p.scale, t.x);
-            v[8 * g + 2 * i + 1] = fmaf(__uint_as_float(r[8 * g + 2 * i + 1]), p.scale, t.y);
+            v[8 * g + 2 * i] = fmaf(__uint_as_float(r[8 * g + 2 * i]), row_scale, t.x);
+            v[8 * g + 2 * i + 1] = fmaf(__uint_as_float(r[8 * g + 2 * i + 1]), row_scale, t.y);
           }
         }
         if (c + 1 < nch) {
@@ -572,7 +588,9 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
   }
   const CUtensorMap& tr = g.has_res ? g.tr : g.tc;
   const CUtensorMap& twt = (PAIR && g.tail_n) ? g.tw_tail : g.tw;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, g.ta, g.tw, twt, g.tc, tr, prm);
+  const CUtensorMap& taa = prm.ln_aug ? g.ta_aug : g.ta;
+  const CUtensorMap& twa = prm.ln_aug ? g.tw_aug : g.tw;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, g.ta, g.tw, twt, g.tc, tr, taa, twa, prm);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return SV_OK;
 }
@@ -655,15 +673,17 @@ int gemm_pick_bn(int M, int N, int K, bool pair) {
   return best;
 }
 
-sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8) {
+sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8,
+                       bool allow_pair) {
   g->M = M;
   g->N = N;
   g->K = K;
   g->fp8 = fp8;
+  g->has_aug = 0;
   // CTA pairs (256-row tiles, half the W traffic per SM, deeper pipelines) for long
   // K (the MLP down-projection). Measured over the whole 27-layer encoder, pairs for
   // every GEMM or for none were 1.5% and 4% slower than pairs for K >= 2048 only.
-  g->mc = (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && K >= 2048;
+  g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && K >= 2048;
   g->bn = gemm_pick_bn(M, N, K, g->mc);
   if (g->mc && g->bn > kPairMaxBn) g->bn = kPairMaxBn;
   // A narrower last column tile (N % bn columns) runs MMAs of its own width, rounded
@@ -716,7 +736,22 @@ sv_status gemm_output_map(CUtensorMap* m, const void* ptr, int M, int N, int e4m
                    box, e4m3 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// The folded LayerNorm's extra K block: [rows, 16] F16 tiles with 32-byte rows in
+// the 32-byte swizzle (the layout the MMA descriptor names).
+sv_status gemm_aug_map(CUtensorMap* m, const void* ptr, int rows, int box_rows) {
+  const uint64_t dims[2] = {16, uint64_t(rows)};
+  const uint64_t strides[1] = {32};
+  const uint32_t box[2] = {16, uint32_t(box_rows)};
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
 sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e) {
+  if (e.ln_r && e.ln_aug_a && e.ln_aug_w && !g->fp8 && !g->mc) {
+    sv_status st = gemm_aug_map(&g->ta_aug, e.ln_aug_a, g->M, kBM);
+    if (st == SV_OK) st = gemm_aug_map(&g->tw_aug, e.ln_aug_w, g->N, g->bn);
+    if (st != SV_OK) return st;
+    g->has_aug = 1;
+  }
   sv_status st = gemm_output_map(&g->tc, e.out, g->M, g->N, e.out_e4m3);
   if (st != SV_OK) return st;
   g->has_res = e.residual != nullptr;
@@ -755,6 +790,12 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.act = e.act;
   p.out_e4m3 = e.out_e4m3;
   p.scale = e.scale;
+  p.ln_r = e.ln_r;
+  p.ln_aug = e.ln_r != nullptr;
+  if (e.ln_r && (!e.ln_aug_a || !e.ln_aug_w || e.pos || g.fp8 || g.mc || !g.has_aug)) {
+    set_error("gemm: a folded LayerNorm needs its extra K block, F16 operands and single-CTA tiles");
+    return SV_ERR_INVALID_ARG;
+  }
   p.err = dev_err();
   const int key = g.bn | (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0);
   switch (key) {

@@ -45,12 +45,21 @@ struct GemmEpi {
   // see attention_blocked_bytes. `out` must still name a buffer of >= M*N f16.
   void* blk_out = nullptr;
   int blk_T = 0, blk_H = 0, blk_B = 0;
+  // LayerNorm of A folded in (A is the LayerNorm input, W already scaled by gamma):
+  // the GEMM runs one more K block of 16, ln_aug_a [M, 16] . ln_aug_w [N, 16]^T =
+  // -mean_m s_n, and the epilogue scales row m by ln_r[m] before adding `bias` (b').
+  // Single-CTA tiles and F16 operands only.
+  const float* ln_r = nullptr;         // [M]
+  const __half* ln_aug_a = nullptr;    // [M, 16]
+  const __half* ln_aug_w = nullptr;    // [N, 16]
 };
 
 // The operand side of a GEMM: tensor maps for A and W plus the sizes.
 struct GemmOperands {
   CUtensorMap ta, tw, tc, tr;  // A, W, output, residual
   CUtensorMap tw_tail;         // W rows of the narrow last column tile (CTA pairs)
+  CUtensorMap ta_aug, tw_aug;  // the extra K block of a folded LayerNorm
+  int has_aug = 0;
   int tail_n = 0;              // MMA N of the narrow last column tile, 0 if all tiles are full
   int tail_last = 0;           // narrow tiles after all full ones in the work order
   int M = 0, N = 0, K = 0;
@@ -67,7 +76,9 @@ struct GemmOperands {
 // 128-byte swizzle the GEMM expects, box [box_rows, 128 bytes].
 sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int fp8, int box_rows);
 int gemm_pick_bn(int M, int N, int K, bool mc);
-sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8);
+// allow_pair = false keeps single-CTA tiles (a folded LayerNorm needs them).
+sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8,
+                       bool allow_pair = true);
 // Builds the output / residual tensor maps for the epilogue's buffers (must precede gemm_launch).
 sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e);
 sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s);
@@ -87,6 +98,13 @@ sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, fl
 // ---- elementwise (elementwise.cu)
 sv_status layernorm_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width,
                            float eps, int out_e4m3, cudaStream_t s);
+// Row statistics only, for a LayerNorm folded into a GEMM: r[m] = 1/sqrt(var + eps)
+// and aug[m, 0..15] = (-mean_hi, -mean_hi, -mean_lo, 0, ...) in F16.
+sv_status ln_stats_launch(const __half* x, float* r, __half* aug, int rows, int width, float eps, cudaStream_t s);
+// W <- W * gamma (per column k, in place, F16); w_aug[n, 0..15] = (s_hi, s_lo, s_hi, 0, ...)
+// with s = sum_k W'[n, k]; b_out[n] = b[n] (0 if null) + sum_k beta[k] W[n, k] (original W), F16.
+sv_status fold_ln_launch(__half* W, const __half* gamma, const __half* beta, const __half* b, __half* w_aug,
+                         __half* b_out, int N, int K, cudaStream_t s);
 sv_status pad_pixels_launch(const __half* pix, void* out, long rows, int P, int Kp, int out_e4m3, cudaStream_t s);
 sv_status quantize_launch(const __half* x, uint8_t* y, size_t n, cudaStream_t s);
 sv_status wait_probe_launch(unsigned int limit_us, cudaStream_t s);
