@@ -25,90 +25,112 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return lo | (hi << 16);
 }
 
-// LayerNorm, one warp per row ("SigLIP ViT benchmark", LayerNorm paragraph):
+// LayerNorm, one half-warp per row ("SigLIP ViT benchmark", LayerNorm paragraph):
 // mean, then the centred (biased) variance, both in F32 from the row held in
-// registers, then the affine map. Each lane owns CPL chunks of 4 values
-// (8-byte loads); a 1152-wide row is 9 chunks per lane. With `stats_r` set only
-// the row statistics are written: 1/sqrt(var + eps) to stats_r and, for the
-// consuming GEMM's extra K block, the F16 row (-mean_hi, -mean_hi, -mean_lo, 0...)
-// to stats_aug (mean_hi + mean_lo = mean to about 2^-22 relative).
+// registers, then the affine map. Each of the 16 lanes owns CPL chunks of 8 values
+// (16-byte loads, all issued before any arithmetic); a 1152-wide row is 9 chunks
+// per lane. With `stats_r` set only the row statistics are written:
+// 1/sqrt(var + eps) to stats_r and, for the consuming GEMM's extra K block, the F16
+// row (-mean_hi, -mean_hi, -mean_lo, 0...) to stats_aug (mean_hi + mean_lo = mean to
+// about 2^-22 relative).
+__device__ __forceinline__ float half_sum(float v) {  // over the 16 lanes of a half-warp
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 template <int CPL>
-__global__ void __launch_bounds__(256) layernorm_kernel(const __half* __restrict__ x, const __half* __restrict__ g,
+__global__ void __launch_bounds__(256, CPL <= 9 ? 4 : 1) layernorm_kernel(const __half* __restrict__ x, const __half* __restrict__ g,
                                                         const __half* __restrict__ bta, void* __restrict__ y,
                                                         int rows, int width, float eps, int out_e4m3,
                                                         float* __restrict__ stats_r, __half* __restrict__ stats_aug) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long row = long(blockIdx.x) * 8 + warp;
-  if (row >= rows) return;
-  const int chunks = width >> 2;
+  const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;  // half-warp (row of the block), its lane
+  const long row0 = long(blockIdx.x) * 16 + hw;
+  const bool live = row0 < rows;
+  const long row = live ? row0 : rows - 1;  // dead half-warps shadow a real row (no stores)
+  const int chunks = width >> 3;
   const __half* xr = x + row * long(width);
-  float v[CPL][4];
+  uint4 u[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = hl + 16 * i;
+    u[i] = c < chunks ? __ldg(reinterpret_cast<const uint4*>(xr) + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
   float s = 0.0f;
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
-    const int c = lane + 32 * i;
-    if (c < chunks) {
-      const uint2 u = *reinterpret_cast<const uint2*>(xr + 4 * c);
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-      v[i][0] = a.x;
-      v[i][1] = a.y;
-      v[i][2] = b.x;
-      v[i][3] = b.y;
-      s += (a.x + a.y) + (b.x + b.y);
-    } else {
-      v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.0f;
+    const __half2* h = reinterpret_cast<const __half2*>(&u[i]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(h[k]);
+      s += f.x + f.y;
     }
   }
-  const float mean = warp_sum(s) / float(width);
+  const float mean = half_sum(s) / float(width);
+  // keep the row as packed halves between passes (re-converting is cheaper than
+  // holding 8 CPL floats live)
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) asm volatile("" : "+r"(u[i].x), "+r"(u[i].y), "+r"(u[i].z), "+r"(u[i].w));
   float q = 0.0f;
 #pragma unroll
   for (int i = 0; i < CPL; ++i)
-    if (lane + 32 * i < chunks) {
+    if (hl + 16 * i < chunks) {
+      const __half2* h = reinterpret_cast<const __half2*>(&u[i]);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float d = v[i][k] - mean;
-        q = fmaf(d, d, q);
+        const float2 f = __half22float2(h[k]);
+        const float d0 = f.x - mean, d1 = f.y - mean;
+        q = fmaf(d0, d0, q);
+        q = fmaf(d1, d1, q);
       }
     }
-  const float var = warp_sum(q) / float(width);
+  const float var = half_sum(q) / float(width);
   const float rstd = rsqrtf(var + eps);
+  if (!live) return;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) asm volatile("" : "+r"(u[i].x), "+r"(u[i].y), "+r"(u[i].z), "+r"(u[i].w));
   if (stats_r) {  // statistics only: the normalisation is folded into the consuming GEMM
-    if (lane < 2) {  // row of the GEMM's extra K block: (-mean_hi, -mean_hi, -mean_lo, 0, ...)
+    if (hl < 2) {  // row of the GEMM's extra K block: (-mean_hi, -mean_hi, -mean_lo, 0, ...)
       const __half hi = __float2half_rn(-mean);
       const __half lo = __float2half_rn(-mean - __half2float(hi));
       const __half2 z = __float2half2_rn(0.0f);
-      uint4 u;  // lane 0: columns 0..7, lane 1: columns 8..15
-      __half2* h = reinterpret_cast<__half2*>(&u);
-      h[0] = lane == 0 ? __halves2half2(hi, hi) : z;
-      h[1] = lane == 0 ? __halves2half2(lo, __float2half_rn(0.0f)) : z;
+      uint4 w;  // lane 0: columns 0..7, lane 1: columns 8..15
+      __half2* h = reinterpret_cast<__half2*>(&w);
+      h[0] = hl == 0 ? __halves2half2(hi, hi) : z;
+      h[1] = hl == 0 ? __halves2half2(lo, __float2half_rn(0.0f)) : z;
       h[2] = h[3] = z;
-      *reinterpret_cast<uint4*>(stats_aug + row * 16 + 8 * lane) = u;
+      *reinterpret_cast<uint4*>(stats_aug + row * 16 + 8 * hl) = w;
     }
-    if (lane == 0) stats_r[row] = rstd;
+    if (hl == 0) stats_r[row] = rstd;
     return;
   }
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
-    const int c = lane + 32 * i;
+    const int c = hl + 16 * i;
     if (c < chunks) {
-      const uint2 gu = __ldg(reinterpret_cast<const uint2*>(g + 4 * c));
-      const uint2 bu = __ldg(reinterpret_cast<const uint2*>(bta + 4 * c));
-      const float2 g0 = __half22float2(*reinterpret_cast<const __half2*>(&gu.x));
-      const float2 g1 = __half22float2(*reinterpret_cast<const __half2*>(&gu.y));
-      const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&bu.x));
-      const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&bu.y));
-      const float o0 = fmaf((v[i][0] - mean) * rstd, g0.x, b0.x);
-      const float o1 = fmaf((v[i][1] - mean) * rstd, g0.y, b0.y);
-      const float o2 = fmaf((v[i][2] - mean) * rstd, g1.x, b1.x);
-      const float o3 = fmaf((v[i][3] - mean) * rstd, g1.y, b1.y);
+      const uint4 gu = __ldg(reinterpret_cast<const uint4*>(g) + c);
+      const uint4 bu = __ldg(reinterpret_cast<const uint4*>(bta) + c);
+      const __half2* xh = reinterpret_cast<const __half2*>(&u[i]);
+      const __half2* gh = reinterpret_cast<const __half2*>(&gu);
+      const __half2* bh = reinterpret_cast<const __half2*>(&bu);
+      float o[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 xv = __half22float2(xh[k]), gv = __half22float2(gh[k]), bv = __half22float2(bh[k]);
+        o[2 * k] = fmaf((xv.x - mean) * rstd, gv.x, bv.x);
+        o[2 * k + 1] = fmaf((xv.y - mean) * rstd, gv.y, bv.y);
+      }
       if (!out_e4m3) {
-        uint2 w;
-        *reinterpret_cast<__half2*>(&w.x) = __floats2half2_rn(o0, o1);
-        *reinterpret_cast<__half2*>(&w.y) = __floats2half2_rn(o2, o3);
-        *reinterpret_cast<uint2*>(static_cast<__half*>(y) + row * long(width) + 4 * c) = w;
+        uint4 w;
+        __half2* wh = reinterpret_cast<__half2*>(&w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) wh[k] = __floats2half2_rn(o[2 * k], o[2 * k + 1]);
+        *reinterpret_cast<uint4*>(static_cast<__half*>(y) + row * long(width) + 8 * c) = w;
       } else {
-        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(y) + row * long(width) + 4 * c) = e4m3x4(o0, o1, o2, o3);
+        uint2 w;
+        w.x = e4m3x4(o[0], o[1], o[2], o[3]);
+        w.y = e4m3x4(o[4], o[5], o[6], o[7]);
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(y) + row * long(width) + 8 * c) = w;
       }
     }
   }
@@ -294,7 +316,7 @@ __global__ void __launch_bounds__(256) fold_ln_kernel(__half* __restrict__ W, co
 template <int CPL>
 void ln_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width, float eps,
                int out_e4m3, float* stats_r, __half* stats_aug, cudaStream_t s) {
-  layernorm_kernel<CPL><<<(rows + 7) / 8, 256, 0, s>>>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug);
+  layernorm_kernel<CPL><<<(rows + 15) / 16, 256, 0, s>>>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug);
 }
 
 }  // namespace
@@ -302,7 +324,7 @@ void ln_launch(const __half* x, const __half* g, const __half* b, void* y, int r
 namespace {
 sv_status ln_any(const __half* x, const __half* g, const __half* b, void* y, int rows, int width, float eps,
                  int out_e4m3, float* stats_r, __half* stats_aug, cudaStream_t s) {
-  const int cpl = (width / 4 + 31) / 32;
+  const int cpl = (width / 8 + 15) / 16;  // 16-byte chunks per lane of a half-warp
   if (cpl <= 1) ln_launch<1>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
   else if (cpl <= 2) ln_launch<2>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
   else if (cpl <= 4) ln_launch<4>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
