@@ -321,7 +321,7 @@ sv_status make_call(GemmCall* c, const void* A, const void* W, int M, int N, int
                     int k_logical) {
   c->e = e;
   c->k = k_logical;
-  SV_TRY(gemm_prepare(&c->g, A, W, M, N, K, fp8, e.ln_r == nullptr));
+  SV_TRY(gemm_prepare(&c->g, A, W, M, N, K, fp8));
   return gemm_bind_epilogue(&c->g, c->e);
 }
 

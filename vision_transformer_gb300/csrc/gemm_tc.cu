@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmWt, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmAa,
-                   const __grid_constant__ CUtensorMap tmWa, const Params p) {
+                   const __grid_constant__ CUtensorMap tmWa, const __grid_constant__ CUtensorMap tmWat,
+                   const Params p) {
   using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_res = bar_drain + 8;  // [4 warps][ring]
 
   // Work items: tiles, or (PAIR) 256-row tiles shared by the two CTAs of a cluster.
-  const int aug_blocks = (!PAIR && !FP8 && p.ln_aug) ? 1 : 0;  // folded LayerNorm's extra K block
+  const int aug_blocks = (!FP8 && p.ln_aug) ? 1 : 0;  // folded LayerNorm's extra K block
   const int rank = PAIR ? int(cluster_ctarank()) : 0;
   const bool leader = rank == 0;
   const int it0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
@@ -238,9 +239,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_u32(smem + stage * C::kStage);
           const int kc = kb * (FP8 ? 128 : 64);
           if (kb == p.k_blocks) {  // folded LayerNorm: the 16-wide K block (-mean | column sums)
-            mbar_arrive_expect_tx(fb, (kBM + BN) * 32);
-            tma_load_2d(sa, &tmAa, fb, 0, mt * kBM);
-            tma_load_2d(sa + C::kStageA, &tmWa, fb, 0, nt * BN);
+            if (PAIR) {  // each CTA: its 128 rows of the A block, its half of the W block's rows
+              const bool narrow = nt == p.n_full && p.tail_n;
+              const int wrows = narrow ? p.tail_n / 2 : BN / 2;
+              const uint32_t fb_lead = mapa_shared(fb, 0);
+              if (leader) mbar_arrive_expect_tx(fb, 2 * (kBM + wrows) * 32);
+              tma_load_2d_pair(sa, &tmAa, fb_lead, 0, mt * kBM);
+              tma_load_2d_pair(sa + C::kStageA, narrow ? &tmWat : &tmWa, fb_lead, 0, nt * BN + rank * wrows);
+            } else {
+              mbar_arrive_expect_tx(fb, (kBM + BN) * 32);
+              tma_load_2d(sa, &tmAa, fb, 0, mt * kBM);
+              tma_load_2d(sa + C::kStageA, &tmWa, fb, 0, nt * BN);
+            }
           } else if (PAIR) {  // both CTAs' copies complete on the leader's barrier
             const uint32_t fb_lead = mapa_shared(fb, 0);
             if (nt == p.n_full && p.tail_n) {  // narrow tile: each CTA holds tail_n / 2 W rows
@@ -307,9 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::kStage);
           const uint32_t sb = sa + C::kStageA;
-          if (!PAIR && !FP8 && kb == p.k_blocks) {
+          if (!FP8 && kb == p.k_blocks) {
             // 32-byte rows with the 32-byte swizzle: 8-row groups 256 bytes apart
-            mma_f16(d, make_sdesc(sa, 16, 256, 6), make_sdesc(sb, 16, 256, 6), idesc, 1u);
+            if (PAIR)
+              mma_f16_pair(d, make_sdesc(sa, 16, 256, 6), make_sdesc(sb, 16, 256, 6), idesc, 1u);
+            else
+              mma_f16(d, make_sdesc(sa, 16, 256, 6), make_sdesc(sb, 16, 256, 6), idesc, 1u);
           } else
 #pragma unroll
           for (int j = 0; j < 4; ++j) {  // 4 instructions x 32 bytes of K
@@ -590,7 +603,8 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
   const CUtensorMap& twt = (PAIR && g.tail_n) ? g.tw_tail : g.tw;
   const CUtensorMap& taa = prm.ln_aug ? g.ta_aug : g.ta;
   const CUtensorMap& twa = prm.ln_aug ? g.tw_aug : g.tw;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, g.ta, g.tw, twt, g.tc, tr, taa, twa, prm);
+  const CUtensorMap& twat = (prm.ln_aug && PAIR && g.tail_n) ? g.tw_aug_tail : twa;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, g.ta, g.tw, twt, g.tc, tr, taa, twa, twat, prm);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return SV_OK;
 }
@@ -681,9 +695,10 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
   g->fp8 = fp8;
   g->has_aug = 0;
   // CTA pairs (256-row tiles, half the W traffic per SM, deeper pipelines) for long
-  // K (the MLP down-projection). Measured over the whole 27-layer encoder, pairs for
-  // every GEMM or for none were 1.5% and 4% slower than pairs for K >= 2048 only.
-  g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && K >= 2048;
+  // K or wide N (the MLP down- and up-projections, QKV): measured on the 27-layer
+  // encoder, about 2% faster than single CTAs there and 1.5% slower on the
+  // 1152 x 1152 output projection.
+  g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && (K >= 2048 || N >= 2048);
   g->bn = gemm_pick_bn(M, N, K, g->mc);
   if (g->mc && g->bn > kPairMaxBn) g->bn = kPairMaxBn;
   // A narrower last column tile (N % bn columns) runs MMAs of its own width, rounded
@@ -746,9 +761,10 @@ sv_status gemm_aug_map(CUtensorMap* m, const void* ptr, int rows, int box_rows) 
 }
 
 sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e) {
-  if (e.ln_r && e.ln_aug_a && e.ln_aug_w && !g->fp8 && !g->mc) {
+  if (e.ln_r && e.ln_aug_a && e.ln_aug_w && !g->fp8) {
     sv_status st = gemm_aug_map(&g->ta_aug, e.ln_aug_a, g->M, kBM);
-    if (st == SV_OK) st = gemm_aug_map(&g->tw_aug, e.ln_aug_w, g->N, g->bn);
+    if (st == SV_OK) st = gemm_aug_map(&g->tw_aug, e.ln_aug_w, g->N, g->mc ? g->bn / 2 : g->bn);
+    if (st == SV_OK && g->mc && g->tail_n) st = gemm_aug_map(&g->tw_aug_tail, e.ln_aug_w, g->N, g->tail_n / 2);
     if (st != SV_OK) return st;
     g->has_aug = 1;
   }
@@ -792,8 +808,8 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.scale = e.scale;
   p.ln_r = e.ln_r;
   p.ln_aug = e.ln_r != nullptr;
-  if (e.ln_r && (!e.ln_aug_a || !e.ln_aug_w || e.pos || g.fp8 || g.mc || !g.has_aug)) {
-    set_error("gemm: a folded LayerNorm needs its extra K block, F16 operands and single-CTA tiles");
+  if (e.ln_r && (!e.ln_aug_a || !e.ln_aug_w || e.pos || g.fp8 || !g.has_aug)) {
+    set_error("gemm: a folded LayerNorm needs its extra K block and F16 operands");
     return SV_ERR_INVALID_ARG;
   }
   p.err = dev_err();

@@ -59,6 +59,7 @@ struct GemmOperands {
   CUtensorMap ta, tw, tc, tr;  // A, W, output, residual
   CUtensorMap tw_tail;         // W rows of the narrow last column tile (CTA pairs)
   CUtensorMap ta_aug, tw_aug;  // the extra K block of a folded LayerNorm
+  CUtensorMap tw_aug_tail;     // its W rows for the narrow last column tile (CTA pairs)
   int has_aug = 0;
   int tail_n = 0;              // MMA N of the narrow last column tile, 0 if all tiles are full
   int tail_last = 0;           // narrow tiles after all full ones in the work order
@@ -76,7 +77,7 @@ struct GemmOperands {
 // 128-byte swizzle the GEMM expects, box [box_rows, 128 bytes].
 sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int fp8, int box_rows);
 int gemm_pick_bn(int M, int N, int K, bool mc);
-// allow_pair = false keeps single-CTA tiles (a folded LayerNorm needs them).
+// allow_pair = false keeps single-CTA tiles.
 sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8,
                        bool allow_pair = true);
 // Builds the output / residual tensor maps for the epilogue's buffers (must precede gemm_launch).
