@@ -106,6 +106,22 @@ sv_status sv_model_dims(int* tokens, int* patch_dim, int* width, int* heads, int
  */
 sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int gemm_dtype, void* stream);
 
+/*
+ * Packs whole images into the patch rows sv_encode takes ("SigLIP ViT
+ * benchmark", image-binding paragraph: the host-side step that views an image
+ * as [batch, patch_y, patch_x, y, x, channel] and flattens it to [batch, 729,
+ * 588]), on the GPU. images: f16 [batch, image_side, image_side, channels]
+ * (row-major, channel fastest; normalisation stays with the caller, as on the
+ * pages); pixels: f16 [batch, (image_side/patch)^2, patch*patch*channels] with
+ * element (y*patch + x)*channels + c of token py*(image_side/patch) + px equal
+ * to pixel (py*patch + y, px*patch + x, c). For So400m/14 at 378 px:
+ * image_side 378, channels 3, patch 14 -> [batch, 729, 588]. A pure layout change.
+ * Requirements: image_side % patch == 0; patch*channels even; pointers 4-byte
+ * aligned. Errors: SV_ERR_INVALID_ARG, SV_ERR_CUDA.
+ */
+sv_status sv_pack_patches(const void* images, void* pixels, int batch, int image_side, int channels, int patch,
+                          void* stream);
+
 /* ---------------------------------------------------------------- per-op */
 
 /*

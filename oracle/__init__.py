@@ -61,10 +61,12 @@ def lib():
                                        ctypes.c_long, ctypes.c_float]
         L.oracle_patch_embed.argtypes = [_FP, _FP, _FP, _FP, _FP, ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                          ctypes.c_long, ctypes.c_int]
+        L.oracle_pack_patches.argtypes = [_FP, _FP, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long]
         L.oracle_map_pool.argtypes = [ctypes.POINTER(Model), _FP, _FP, ctypes.c_long, ctypes.c_int]
         L.oracle_encode.argtypes = [ctypes.POINTER(Model), _FP, _FP, ctypes.c_long, ctypes.c_int, ctypes.c_int, _FP]
         for f in ("oracle_gelu", "oracle_softmax_rows", "oracle_linear", "oracle_layernorm", "oracle_attention",
-                  "oracle_patch_embed", "oracle_map_pool", "oracle_encode", "oracle_set_threads"):
+                  "oracle_patch_embed", "oracle_pack_patches", "oracle_map_pool", "oracle_encode",
+                  "oracle_set_threads"):
             getattr(L, f).restype = None
         _lib = L
     return _lib
@@ -127,6 +129,17 @@ def attention(q, k, v, heads: int, head_dim: int, scale: float | None = None) ->
     s = 1.0 / np.sqrt(head_dim) if scale is None else scale
     lib().oracle_attention(_p(q), _p(k), _p(v), _p(o), B, heads, T, head_dim, s)
     return o
+
+
+def pack_patches(img, patch: int = 14) -> np.ndarray:
+    """[B, side, side, C] images -> [B, (side/patch)^2, patch*patch*C] patch rows."""
+    img = _f32(img)
+    B, S, S2, C = img.shape
+    assert S == S2 and S % patch == 0
+    G = S // patch
+    pix = np.empty((B, G * G, patch * patch * C), dtype=np.float32)
+    lib().oracle_pack_patches(_p(img), _p(pix), B, S, C, patch)
+    return pix
 
 
 def patch_embed(pix, Wp, bp, pos, fp8: bool = False) -> np.ndarray:

@@ -257,6 +257,23 @@ void oracle_attention(const float* q, const float* k, const float* v, float* o, 
   });
 }
 
+// Host packing of whole images into patch rows ("SigLIP ViT benchmark", image-binding
+// paragraph: the image is viewed as [batch, patch_y, patch_x, y, x, channel] and
+// flattened to [batch, patches, patch_dim]): token t = py * G + px with G = side / p,
+// element k = (y * p + x) * C + c of that token is pixel (py * p + y, px * p + x,
+// channel c) of the side x side x C image (channel fastest, row-major).
+void oracle_pack_patches(const float* img, float* pix, long B, long side, long C, long p) {
+  const long G = side / p, T = G * G, P = p * p * C;
+  for (long b = 0; b < B; ++b)
+    for (long py = 0; py < G; ++py)
+      for (long px = 0; px < G; ++px)
+        for (long y = 0; y < p; ++y)
+          for (long x = 0; x < p; ++x)
+            for (long c = 0; c < C; ++c)
+              pix[(b * T + py * G + px) * P + (y * p + x) * C + c] =
+                  img[((b * side + py * p + y) * side + px * p + x) * C + c];
+}
+
 // X[B][T][D] = pix[B][T][P] Wp[P][D] + bp + pos[T][D]
 void oracle_patch_embed(const float* pix, const float* Wp, const float* bp, const float* pos, float* X, long B,
                         long T, long P, long D, int fp8) {

@@ -161,6 +161,19 @@ def test_ln_gemm_folded(sv, M, N, K, act):
     assert torch.equal(C, C2)
 
 
+@pytest.mark.parametrize("B,side,C,patch", [(2, 378, 3, 14), (1, 42, 3, 14), (3, 32, 4, 8)])
+def test_pack_patches_bit_exact(sv, B, side, C, patch):
+    """Image -> patch-row packing (image-binding paragraph) is a permutation of F16
+    values: bit-exact against the oracle's packing."""
+    img = synth.uniform(80, side, (B, side, side, C)).astype(np.float16)
+    G = side // patch
+    out = torch.full((B, G * G, patch * patch * C), float("nan"), dtype=torch.float16, device="cuda")
+    sv.sv_pack_patches(dev_f16(img), out, B, side, C, patch)
+    sv.sv_sync()
+    ref = oracle.pack_patches(img.astype(np.float32), patch).astype(np.float16)
+    assert np.array_equal(host(out).astype(np.float16).view(np.uint16), ref.view(np.uint16))
+
+
 def _attn_ref(qkv, H):
     D = H * 72
     return oracle.attention(qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:], H, 72)

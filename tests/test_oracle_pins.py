@@ -53,6 +53,24 @@ def test_patch_embed_is_valid_stride14_convolution(hw):
     np.testing.assert_allclose(got, t[0].permute(1, 2, 0).reshape(-1, D).numpy(), rtol=1e-5, atol=1e-5)
 
 
+@pytest.mark.parametrize("side", [28, 42])
+def test_pack_then_embed_is_the_patch_convolution(side):
+    """The oracle's image packing followed by its embedding GEMM equals torch's
+    14x14 stride-14 convolution of the images (float64): a wrong token order, a
+    transposed patch or a channel-order slip in the packing would fail this."""
+    D, B = 8, 2
+    img = synth.uniform(6, 100, (B, side, side, 3)).astype(np.float64)
+    Wp = synth.normal(6, 101, (588, D), std=0.05).astype(np.float64)
+    bp = synth.normal(6, 102, (D,), std=0.01).astype(np.float64)
+    pix = oracle.pack_patches(img)
+    assert pix.shape == (B, (side // PATCH) ** 2, 588)
+    got = oracle.patch_embed(pix, Wp, bp, np.zeros((pix.shape[1], D)))
+    Wk = Wp.reshape(PATCH, PATCH, 3, D)
+    t = F.conv2d(torch.from_numpy(img).permute(0, 3, 1, 2), torch.from_numpy(Wk).permute(3, 2, 0, 1),
+                 torch.from_numpy(bp), stride=PATCH)
+    np.testing.assert_allclose(got, t.permute(0, 2, 3, 1).reshape(B, -1, D).numpy(), rtol=1e-5, atol=1e-5)
+
+
 def test_patch_embed_adds_position_per_token():
     pix = synth.uniform(6, 1, (2, 4, 588))
     Wp = synth.normal(6, 2, (588, 8), std=0.05)

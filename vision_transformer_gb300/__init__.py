@@ -35,6 +35,7 @@ SIGNATURES = [
     ("sv_gemm_bias_act", _I, [_VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     ("sv_layernorm", _I, [_VP, _VP, _VP, _VP, _I, _I, _F, _I, _VP]),
     ("sv_ln_gemm", _I, [_VP, _VP, _VP, _F, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
+    ("sv_pack_patches", _I, [_VP, _VP, _I, _I, _I, _I, _VP]),
     ("sv_attention", _I, [_VP, _VP, _I, _I, _I, _I, _F, _I, _VP]),
     ("sv_map_pool", _I, [_VP, _VP, _I, _I, _VP]),
     ("sv_map_pool_static", _I, [_VP, _VP, _I, _I, _VP]),
@@ -121,6 +122,12 @@ def sv_gemm_bias_act(A, W, bias, pos, pos_rows: int, residual, C, M: int, N: int
     _check("sv_gemm_bias_act", load().sv_gemm_bias_act(_ptr(A), _ptr(W), _ptr(bias), _ptr(pos), pos_rows,
                                                        _ptr(residual), _ptr(C), M, N, K, act, in_dtype, out_dtype,
                                                        scale, _stream(stream)))
+
+
+def sv_pack_patches(images, pixels, batch: int, image_side: int = 378, channels: int = 3, patch: int = 14,
+                    stream=None):
+    _check("sv_pack_patches", load().sv_pack_patches(_ptr(images), _ptr(pixels), batch, image_side, channels, patch,
+                                                     _stream(stream)))
 
 
 def sv_ln_gemm(x, gamma, beta, W, bias, C, M: int, N: int, K: int, act: int = 0, eps: float = 1e-6, stream=None):

@@ -762,6 +762,25 @@ sv_status sv_ln_gemm(const void* x, const void* gamma, const void* beta, float e
   return run_gemm(c, s);
 }
 
+sv_status sv_pack_patches(const void* images, void* pixels, int batch, int image_side, int channels, int patch,
+                          void* stream) {
+  if (!images || !pixels || batch < 1 || patch < 1 || channels < 1 || image_side < patch || image_side % patch ||
+      (patch * channels) % 2 || image_side > 65536) {
+    set_error("sv_pack_patches: bad arguments (side %d must be a multiple of patch %d; patch * channels even)",
+              image_side, patch);
+    return SV_ERR_INVALID_ARG;
+  }
+  if (!aligned(images, 4) || !aligned(pixels, 4)) {
+    set_error("sv_pack_patches: pointers must be 4-byte aligned");
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_TRY(ensure_runtime());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch L(kKindOther, 0.0, double(batch) * image_side * image_side * channels * 4.0, s);
+  return pack_patches_launch(static_cast<const __half*>(images), static_cast<__half*>(pixels), batch, image_side,
+                             channels, patch, s);
+}
+
 sv_status sv_layernorm(const void* x, const void* gamma, const void* beta, void* y, int rows, int width, float eps,
                        int out_dtype, void* stream) {
   if (!x || !gamma || !beta || !y || rows < 1 || width < 8 || width > 4096 || width % 8 || !(eps >= 0.0f) ||

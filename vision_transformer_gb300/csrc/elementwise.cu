@@ -136,6 +136,27 @@ __global__ void __launch_bounds__(256, CPL <= 9 ? 4 : 1) layernorm_kernel(const 
   }
 }
 
+// Whole images [B, side, side, C] f16 (channel fastest) -> patch rows
+// [B, G*G, p*p*C] f16 with G = side / p ("SigLIP ViT benchmark", image-binding
+// paragraph: [batch, patch_y, patch_x, y, x, channel] flattened): element
+// k = (y p + x) C + c of token py G + px is pixel (py p + y, px p + x, c). A token's
+// p*C-value run for one patch row y is contiguous in both layouts, so one thread
+// moves two values (p*C is even for the 3-channel images of the path).
+__global__ void pack_patches_kernel(const __half2* __restrict__ img, __half2* __restrict__ pix, long pairs, int side,
+                                    int C, int p) {
+  const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= pairs) return;
+  const int G = side / p, P = p * p * C, run = p * C;
+  const long e = 2 * i;  // first output element of the pair
+  const long row = e / P;
+  const int k = int(e - row * P);
+  const long b = row / (long(G) * G);
+  const int t = int(row - b * G * G), py = t / G, px = t - (t / G) * G;
+  const int y = k / run, r = k - y * run;  // r: offset inside the run of patch row y
+  const long src = ((b * side + py * p + y) * long(side) + px * p) * C + r;
+  pix[i] = img[src >> 1];
+}
+
 // Pixels [rows, P] f16 -> GEMM operand [rows, Kp] (f16 or e4m3 codes), zero
 // columns P..Kp-1 (the K tail both GEMM operands share). One thread per 4 values.
 __global__ void pad_pixels_kernel(const __half* __restrict__ pix, void* __restrict__ out, long rows, int P, int Kp,
@@ -355,6 +376,14 @@ sv_status fold_ln_launch(__half* W, const __half* g, const __half* be, const __h
   fold_ln_kernel<<<unsigned((N + 7) / 8), 256, 0, s>>>(W, g, be, b, w_aug, b_out, N, K);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "fold_ln launch");
+}
+
+sv_status pack_patches_launch(const __half* img, __half* pix, int B, int side, int C, int p, cudaStream_t s) {
+  const long pairs = long(B) * side * side * C / 2;
+  pack_patches_kernel<<<unsigned((pairs + 255) / 256), 256, 0, s>>>(reinterpret_cast<const __half2*>(img),
+                                                                   reinterpret_cast<__half2*>(pix), pairs, side, C, p);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "pack_patches launch");
 }
 
 sv_status pad_pixels_launch(const __half* pix, void* out, long rows, int P, int Kp, int out_e4m3, cudaStream_t s) {

@@ -80,6 +80,7 @@ struct Params {
   const float* ln_r;
   int ln_aug;
   int* err;
+  void* out;  // the output matrix [M, N] (also described by the output tensor map)
   // head-blocked output (fused QKV projection feeding attention), or null
   uint8_t* blk;
   int blk_T, blk_H, blk_B, blk_tiles;
@@ -798,6 +799,7 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.pos = e.pos;
   p.pos_rows = e.pos_rows > 0 ? e.pos_rows : 1;
   p.has_res = e.residual != nullptr;
+  p.out = e.out;
   p.blk = static_cast<uint8_t*>(e.blk_out);
   p.blk_T = e.blk_T;
   p.blk_H = e.blk_H;

@@ -106,6 +106,7 @@ sv_status ln_stats_launch(const __half* x, float* r, __half* aug, int rows, int 
 // with s = sum_k W'[n, k]; b_out[n] = b[n] (0 if null) + sum_k beta[k] W[n, k] (original W), F16.
 sv_status fold_ln_launch(__half* W, const __half* gamma, const __half* beta, const __half* b, __half* w_aug,
                          __half* b_out, int N, int K, cudaStream_t s);
+sv_status pack_patches_launch(const __half* img, __half* pix, int B, int side, int C, int p, cudaStream_t s);
 sv_status pad_pixels_launch(const __half* pix, void* out, long rows, int P, int Kp, int out_e4m3, cudaStream_t s);
 sv_status quantize_launch(const __half* x, uint8_t* y, size_t n, cudaStream_t s);
 sv_status wait_probe_launch(unsigned int limit_us, cudaStream_t s);
