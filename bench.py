@@ -7,7 +7,7 @@ encoder + MAP at 378 px, F16 GEMM operands, batch 32 per GPU (the regime the
 tensor-core target is quoted in); weights are drawn by the seeded generator
 and resident in HBM; pixels are uniform in [-1, 1].
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--dtype f16|e4m3]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--dtype f16|e4m3] [--unfused-qkv]
   python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
 Prints one JSON line (rank 0). Multi-GPU runs (torchrun, one rank per GPU)
@@ -181,6 +181,7 @@ def config(args, world):
                         f"batch {args.batch} per GPU",
             "global_batch": args.batch * world, "layers": L27, "tokens": T, "width": D,
             "gemm_dtype": args.dtype, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "qkv": "three GEMMs" if getattr(args, "unfused_qkv", False) else "one fused GEMM",
             "l2": "no flush: every step streams 0.85 GB of F16 weights and several GB of activations, "
                   "far above the 129 MB L2"}
 
@@ -192,6 +193,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--batch", type=int, default=32, help="images per GPU per step")
     ap.add_argument("--dtype", choices=("f16", "e4m3"), default="f16")
+    ap.add_argument("--unfused-qkv", action="store_true", help="Q, K, V as three GEMMs (comparison only)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-layers", type=int, default=4, help="layers in the timed oracle sample")
@@ -228,8 +230,10 @@ def main():
     out = torch.empty(count, 1, D, dtype=torch.float16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    flags = vt.SV_ENCODE_UNFUSED_QKV if args.unfused_qkv else 0
+
     def step():
-        vt.sv_encode(pix, out, count, L27, gdt, stream)
+        vt.sv_encode_ex(pix, out, count, L27, gdt, flags, stream)
 
     for _ in range(args.warmup):
         step()

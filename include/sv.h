@@ -106,6 +106,23 @@ sv_status sv_model_dims(int* tokens, int* patch_dim, int* width, int* heads, int
  */
 sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int gemm_dtype, void* stream);
 
+/* Options of sv_encode_ex. */
+typedef enum {
+  /* Q, K and V as three 1152 -> 1152 GEMMs over the row slices of the fused
+   * weight instead of one 1152 -> 3456 GEMM (the pages' fused-QKV comparison:
+   * "Fused QKV projection" section, which measured fusion as about 7.6% faster).
+   * The results are the same; only the launch structure differs. */
+  SV_ENCODE_UNFUSED_QKV = 1
+} sv_encode_flags;
+
+/*
+ * sv_encode with options: flags is 0 (exactly sv_encode) or SV_ENCODE_UNFUSED_QKV.
+ * Each (batch, gemm_dtype, flags) combination has its own cached workspace.
+ * Errors: as sv_encode; unknown flag bits -> SV_ERR_INVALID_ARG.
+ */
+sv_status sv_encode_ex(const void* pixels, void* out, int batch, int layers, int gemm_dtype, int flags,
+                       void* stream);
+
 /*
  * Packs whole images into the patch rows sv_encode takes ("SigLIP ViT
  * benchmark", image-binding paragraph: the host-side step that views an image

@@ -66,6 +66,8 @@ def test_errors_before_device_work(lib):
         vt.SV_ERR_INVALID_ARG
     assert lib.sv_gemm_bias_act(p16, p16, None, None, 1, None, p16, 16, 16, 16, 0, 3, 0, 1.0, None) == \
         vt.SV_ERR_INVALID_ARG
+    # image packing: side not a multiple of the patch
+    assert lib.sv_pack_patches(p16, p16, 1, 30, 3, 14, None) == vt.SV_ERR_INVALID_ARG
     # LayerNorm folded into a GEMM: K beyond the LayerNorm's 4096, or N not a multiple of 16
     assert lib.sv_ln_gemm(p16, p16, p16, 1e-6, p16, None, p16, 16, 16, 8192, 0, None) == vt.SV_ERR_INVALID_ARG
     assert lib.sv_ln_gemm(p16, p16, p16, 1e-6, p16, None, p16, 16, 24, 16, 0, None) == vt.SV_ERR_INVALID_ARG

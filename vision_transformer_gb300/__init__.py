@@ -32,6 +32,7 @@ SIGNATURES = [
     ("sv_init_weights_dims", _I, [_U64, _I, _I, _I, _I, _I, _I]),
     ("sv_model_dims", _I, [_IP, _IP, _IP, _IP, _IP, _IP]),
     ("sv_encode", _I, [_VP, _VP, _I, _I, _I, _VP]),
+    ("sv_encode_ex", _I, [_VP, _VP, _I, _I, _I, _I, _VP]),
     ("sv_gemm_bias_act", _I, [_VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     ("sv_layernorm", _I, [_VP, _VP, _VP, _VP, _I, _I, _F, _I, _VP]),
     ("sv_ln_gemm", _I, [_VP, _VP, _VP, _F, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
@@ -111,6 +112,14 @@ def sv_model_dims() -> dict:
     vals = [ctypes.c_int() for _ in range(6)]
     _check("sv_model_dims", load().sv_model_dims(*[ctypes.byref(v) for v in vals]))
     return dict(zip(("tokens", "patch_dim", "width", "heads", "mlp", "layers"), (v.value for v in vals)))
+
+
+SV_ENCODE_UNFUSED_QKV = 1
+
+
+def sv_encode_ex(pixels, out, batch: int, layers: int, gemm_dtype: int = SV_GEMM_F16, flags: int = 0, stream=None):
+    _check("sv_encode_ex", load().sv_encode_ex(_ptr(pixels), _ptr(out), batch, layers, gemm_dtype, flags,
+                                               _stream(stream)))
 
 
 def sv_encode(pixels, out, batch: int, layers: int, gemm_dtype: int = SV_GEMM_F16, stream=None):

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <tuple>
 #include <memory>
 #include <string>
 #include <utility>
@@ -117,6 +118,7 @@ struct MapPlan {
 // Workspace and operand maps of the whole forward pass for one batch size and dtype.
 struct Plan {
   int B = 0, fp8 = 0;
+  int qkv_calls = 1;     // GEMMs per layer for Q, K, V: 1 fused, or 3 (SV_ENCODE_UNFUSED_QKV)
   bool fold_ln = false;  // LN1 / LN2 folded into the QKV / MLP-up GEMMs (F16 operands)
   void* mem = nullptr;
   size_t bytes = 0;
@@ -132,7 +134,7 @@ struct Plan {
   std::vector<GemmCall> qkv, out, fc1, fc2;
   MapPlan map;
 };
-std::map<std::pair<int, int>, std::unique_ptr<Plan>> g_plans;      // sv_encode
+std::map<std::tuple<int, int, int>, std::unique_ptr<Plan>> g_plans;  // sv_encode: (batch, dtype, flags)
 std::map<std::pair<int, int>, std::unique_ptr<Plan>> g_map_plans;  // sv_map_pool
 void* g_attn_scratch = nullptr;  // head-blocked copy of sv_attention's input
 size_t g_attn_scratch_bytes = 0;
@@ -378,8 +380,8 @@ sv_status alloc_carved(Carver& c, void** mem, size_t* bytes) {
   return SV_OK;
 }
 
-sv_status get_plan(int B, int fp8, Plan** out) {
-  const auto key = std::make_pair(B, fp8);
+sv_status get_plan(int B, int fp8, int flags, Plan** out) {
+  const auto key = std::make_tuple(B, fp8, flags);
   auto it = g_plans.find(key);
   if (it != g_plans.end()) {
     *out = it->second.get();
@@ -390,6 +392,7 @@ sv_status get_plan(int B, int fp8, Plan** out) {
   std::unique_ptr<Plan> p(new Plan());
   p->B = B;
   p->fp8 = fp8;
+  p->qkv_calls = (flags & SV_ENCODE_UNFUSED_QKV) ? 3 : 1;
   p->fold_ln = !fp8;
   Carver c{nullptr};
   for (int pass = 0; pass < 2; ++pass) {
@@ -420,7 +423,7 @@ sv_status get_plan(int B, int fp8, Plan** out) {
   pe.pos_rows = d.T;
   if ((st = make_call(&p->patch, p->A0, fp8 ? (const void*)g_w.patch_w8 : g_w.patch_w, Mi, d.D, d.Kp, fp8, pe, d.P)))
     return fail(st);
-  p->qkv.resize(size_t(d.L));
+  p->qkv.resize(size_t(d.L) * size_t(p->qkv_calls));
   p->out.resize(size_t(d.L));
   p->fc1.resize(size_t(d.L));
   p->fc2.resize(size_t(d.L));
@@ -429,20 +432,33 @@ sv_status get_plan(int B, int fp8, Plan** out) {
     const size_t i = size_t(l);
     // F16: LN1 / LN2 folded into the QKV / MLP-up GEMMs, which read X itself; E4M3:
     // the LayerNorm kernels write the quantised operand Y
-    GemmEpi qe = epi(p->fold_ln ? w.qkv_bf : w.qkv_b, p->QKV, sc);
     GemmEpi fe = epi(p->fold_ln ? w.fc1_bf : w.fc1_b, p->Hh, sc, SV_ACT_GELU_TANH, fp8);
     if (p->fold_ln) {
-      qe.ln_r = fe.ln_r = p->ln_r;
-      qe.ln_aug_a = fe.ln_aug_a = p->ln_aug;
-      qe.ln_aug_w = w.qkv_aug;
+      fe.ln_r = p->ln_r;
+      fe.ln_aug_a = p->ln_aug;
       fe.ln_aug_w = w.fc1_aug;
     }
-    qe.blk_out = p->QKV;
-    qe.blk_T = d.T;
-    qe.blk_H = d.H;
-    qe.blk_B = B;
     const void* ln_in = p->fold_ln ? static_cast<const void*>(p->X) : p->Y;
-    if ((st = make_call(&p->qkv[i], ln_in, fp8 ? (const void*)w.qkv_w8 : w.qkv_w, Mi, 3 * d.D, d.D, fp8, qe, d.D)) ||
+    // Q, K, V: one fused GEMM over the [3D, D] weight, or (SV_ENCODE_UNFUSED_QKV) three
+    // over its row slices, each writing its third of the head-blocked layout
+    const int nq = p->qkv_calls, wq = 3 * d.D / nq;
+    for (int j = 0; j < nq && st == SV_OK; ++j) {
+      const size_t r0 = size_t(j) * wq;  // first weight row (output column) of this GEMM
+      GemmEpi qe = epi((p->fold_ln ? w.qkv_bf : w.qkv_b) + r0, p->QKV, sc);
+      if (p->fold_ln) {
+        qe.ln_r = p->ln_r;
+        qe.ln_aug_a = p->ln_aug;
+        qe.ln_aug_w = w.qkv_aug + r0 * 16;
+      }
+      qe.blk_out = p->QKV;
+      qe.blk_T = d.T;
+      qe.blk_H = d.H;
+      qe.blk_B = B;
+      qe.blk_col0 = int(r0);
+      const void* wptr = fp8 ? static_cast<const void*>(w.qkv_w8 + r0 * d.D) : static_cast<const void*>(w.qkv_w + r0 * d.D);
+      st = make_call(&p->qkv[i * size_t(nq) + size_t(j)], ln_in, wptr, Mi, wq, d.D, fp8, qe, d.D);
+    }
+    if (st ||
         (st = make_call(&p->out[i], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8,
                         epi(w.out_b, p->X, sc, SV_ACT_NONE, 0, p->X), d.D)) ||
         (st = make_call(&p->fc1[i], ln_in, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8, fe, d.D)) ||
@@ -516,7 +532,7 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
     const LayerW& w = g_w.layers[size_t(l)];
     const size_t i = size_t(l);
     SV_TRY(p.fold_ln ? run_ln_stats(p.X, p.ln_r, p.ln_aug, M, s) : run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
-    SV_TRY(run_gemm(p.qkv[i], s));
+    for (int j = 0; j < p.qkv_calls; ++j) SV_TRY(run_gemm(p.qkv[i * size_t(p.qkv_calls) + size_t(j)], s));
     {
       Launch L(kKindAttn, 4.0 * B * d.H * double(d.T) * double(d.T) * 72.0,
                double(M) * 3 * d.D * 2.0 + double(M) * d.D * (fp8 ? 1.0 : 2.0), s);
@@ -658,12 +674,13 @@ sv_status sv_model_dims(int* tokens, int* patch_dim, int* width, int* heads, int
   return SV_OK;
 }
 
-sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int gemm_dtype, void* stream) {
+sv_status sv_encode_ex(const void* pixels, void* out, int batch, int layers, int gemm_dtype, int flags,
+                       void* stream) {
   SV_TRY(check_ready());
   if (!pixels || !out || batch < 1 || layers < 1 || layers > g_w.d.L ||
-      (gemm_dtype != SV_GEMM_F16 && gemm_dtype != SV_GEMM_E4M3)) {
-    set_error("sv_encode: bad arguments (batch %d, layers %d of %d, gemm_dtype %d)", batch, layers, g_w.d.L,
-              gemm_dtype);
+      (gemm_dtype != SV_GEMM_F16 && gemm_dtype != SV_GEMM_E4M3) || (flags & ~SV_ENCODE_UNFUSED_QKV)) {
+    set_error("sv_encode: bad arguments (batch %d, layers %d of %d, gemm_dtype %d, flags %d)", batch, layers,
+              g_w.d.L, gemm_dtype, flags);
     return SV_ERR_INVALID_ARG;
   }
   if (!aligned(pixels, 8) || !aligned(out, 16)) {
@@ -675,9 +692,13 @@ sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int ge
     return SV_ERR_INVALID_ARG;
   }
   Plan* p = nullptr;
-  SV_TRY(get_plan(batch, gemm_dtype, &p));
+  SV_TRY(get_plan(batch, gemm_dtype, flags, &p));
   return encode(*p, static_cast<const __half*>(pixels), static_cast<__half*>(out), layers,
                 static_cast<cudaStream_t>(stream));
+}
+
+sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int gemm_dtype, void* stream) {
+  return sv_encode_ex(pixels, out, batch, layers, gemm_dtype, 0, stream);
 }
 
 sv_status sv_gemm_bias_act(const void* A, const void* W, const void* bias, const void* pos, int pos_rows,
@@ -978,7 +999,7 @@ sv_status sv_debug_fill_workspace(int batch, int gemm_dtype, int byte_value) {
     return SV_ERR_INVALID_ARG;
   }
   Plan* p = nullptr;
-  SV_TRY(get_plan(batch, gemm_dtype, &p));
+  SV_TRY(get_plan(batch, gemm_dtype, 0, &p));
   SV_CHECK_CUDA(cudaMemset(p->mem, byte_value & 0xFF, p->bytes), "sv_debug_fill_workspace");
   SV_CHECK_CUDA(cudaDeviceSynchronize(), "sv_debug_fill_workspace");
   return SV_OK;

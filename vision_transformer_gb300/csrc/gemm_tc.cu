@@ -84,6 +84,7 @@ struct Params {
   // head-blocked output (fused QKV projection feeding attention), or null
   uint8_t* blk;
   int blk_T, blk_H, blk_B, blk_tiles;
+  int blk_col0;  // first column of the fused [Q | K | V] space this GEMM's columns start at
 };
 
 // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), with
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int g = 0; g < 4; ++g)
               if (g < ngroups) {
-                const int col = n + 8 * g;
+                const int col = p.blk_col0 + n + 8 * g;
                 const int which = col >= 2 * D ? 2 : (col >= D ? 1 : 0);
                 const int rem = col - which * D;
                 const int h = (rem * 58255) >> 22;  // rem / 72, exact for rem < 4096
@@ -804,6 +805,7 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.blk_T = e.blk_T;
   p.blk_H = e.blk_H;
   p.blk_B = e.blk_B;
+  p.blk_col0 = e.blk_col0;
   p.blk_tiles = (e.blk_T + 127) / 128;
   p.act = e.act;
   p.out_e4m3 = e.out_e4m3;

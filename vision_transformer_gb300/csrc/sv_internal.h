@@ -45,6 +45,7 @@ struct GemmEpi {
   // see attention_blocked_bytes. `out` must still name a buffer of >= M*N f16.
   void* blk_out = nullptr;
   int blk_T = 0, blk_H = 0, blk_B = 0;
+  int blk_col0 = 0;  // this GEMM's column 0 is column blk_col0 of the fused [Q | K | V] output
   // LayerNorm of A folded in (A is the LayerNorm input, W already scaled by gamma):
   // the GEMM runs one more K block of 16, ln_aug_a [M, 16] . ln_aug_w [N, 16]^T =
   // -mean_m s_n, and the epilogue scales row m by ln_r[m] before adding `bias` (b').
