@@ -62,10 +62,12 @@ def lib():
         L.oracle_patch_embed.argtypes = [_FP, _FP, _FP, _FP, _FP, ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                          ctypes.c_long, ctypes.c_int]
         L.oracle_pack_patches.argtypes = [_FP, _FP, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long]
+        L.oracle_attention_qk8.argtypes = [_FP, _FP, _FP, _FP, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                           ctypes.c_long, ctypes.c_float]
         L.oracle_map_pool.argtypes = [ctypes.POINTER(Model), _FP, _FP, ctypes.c_long, ctypes.c_int]
         L.oracle_encode.argtypes = [ctypes.POINTER(Model), _FP, _FP, ctypes.c_long, ctypes.c_int, ctypes.c_int, _FP]
         for f in ("oracle_gelu", "oracle_softmax_rows", "oracle_linear", "oracle_layernorm", "oracle_attention",
-                  "oracle_patch_embed", "oracle_pack_patches", "oracle_map_pool", "oracle_encode",
+                  "oracle_patch_embed", "oracle_pack_patches", "oracle_attention_qk8", "oracle_map_pool", "oracle_encode",
                   "oracle_set_threads"):
             getattr(L, f).restype = None
         _lib = L
@@ -121,13 +123,15 @@ def layernorm(x, g, b, eps: float = 1e-6) -> np.ndarray:
     return y
 
 
-def attention(q, k, v, heads: int, head_dim: int, scale: float | None = None) -> np.ndarray:
-    """q, k, v: [B, T, heads*head_dim] token-major; returns o in the same layout."""
+def attention(q, k, v, heads: int, head_dim: int, scale: float | None = None, qk_fp8: bool = False) -> np.ndarray:
+    """q, k, v: [B, T, heads*head_dim] token-major; returns o in the same layout.
+    qk_fp8: Q and K rounded to E4M3 values (scale 2^-4) before the scores."""
     q, k, v = _f32(q), _f32(k), _f32(v)
     B, T, _ = q.shape
     o = np.empty_like(q)
     s = 1.0 / np.sqrt(head_dim) if scale is None else scale
-    lib().oracle_attention(_p(q), _p(k), _p(v), _p(o), B, heads, T, head_dim, s)
+    f = lib().oracle_attention_qk8 if qk_fp8 else lib().oracle_attention
+    f(_p(q), _p(k), _p(v), _p(o), B, heads, T, head_dim, s)
     return o
 
 
@@ -182,13 +186,17 @@ class OracleModel:
         import synth
         return cls(synth.model(seed, dims), dims.tokens, dims.patch_dim, dims.width, dims.heads, dims.mlp)
 
-    def encode(self, pix, layers: int | None = None, fp8: bool = False, want_xf: bool = False):
+    def encode(self, pix, layers: int | None = None, fp8: bool = False, want_xf: bool = False,
+               fp8_attention: bool = False):
+        """fp8: dense-GEMM operands rounded to E4M3; fp8_attention: Q and K rounded to E4M3
+        before the attention scores."""
         pix = _f32(pix)
         B = pix.shape[0]
         L = self.layers if layers is None else layers
         out = np.empty((B, self.width), dtype=np.float32)
         xf = np.empty((B, self.tokens, self.width), dtype=np.float32) if want_xf else None
-        lib().oracle_encode(ctypes.byref(self.struct), _p(pix), _p(out), B, L, int(fp8), _p(xf))
+        mode = (1 if fp8 else 0) | (2 if fp8_attention else 0)
+        lib().oracle_encode(ctypes.byref(self.struct), _p(pix), _p(out), B, L, mode, _p(xf))
         return (out, xf) if want_xf else out
 
     def map_pool(self, xf, fp8: bool = False) -> np.ndarray:

@@ -257,6 +257,21 @@ void oracle_attention(const float* q, const float* k, const float* v, float* o, 
   });
 }
 
+// Attention with FP8 score products ("FP8 attention and resident image/embedding
+// transfers": the QK product on E4M3 operands at scale 2^-4, written quantised by their
+// producer): Q and K are rounded to E4M3 values (q_hat = E4M3(16 q) / 16) before the
+// scores; softmax and the P V product are as in oracle_attention.
+void oracle_attention_qk8(const float* q, const float* k, const float* v, float* o, long B, long H, long T, long dh,
+                          float scale) {
+  const size_t n = size_t(B) * size_t(T) * size_t(H * dh);
+  std::vector<float> q8(n), k8(n);
+  for (size_t i = 0; i < n; ++i) {
+    q8[i] = e4m3_value(16.0f * q[i]) / 16.0f;
+    k8[i] = e4m3_value(16.0f * k[i]) / 16.0f;
+  }
+  oracle_attention(q8.data(), k8.data(), v, o, B, H, T, dh, scale);
+}
+
 // Host packing of whole images into patch rows ("SigLIP ViT benchmark", image-binding
 // paragraph: the image is viewed as [batch, patch_y, patch_x, y, x, channel] and
 // flattened to [batch, patches, patch_dim]): token t = py * G + px with G = side / p,
@@ -307,10 +322,13 @@ void oracle_map_pool(const oracle_model* m, const float* xf, float* out, long B,
 
 // Whole encoder: pix[B][T][P] -> out[B][D] (the [B,1,D] pooled embedding).
 // If xf_out is non-null it receives the final-LN output [B][T][D].
+// fp8 bit 0: dense-GEMM operands rounded to E4M3 (the FP8 GEMM mode); bit 1: Q and K
+// rounded to E4M3 before the attention scores (FP8 attention products).
 void oracle_encode(const oracle_model* m, const float* pix, float* out, long B, int layers, int fp8,
                    float* xf_out) {
   const long T = m->tokens, D = m->width, F = m->mlp, H = m->heads, dh = m->head_dim, M = B * T;
-  const bool q8 = fp8 != 0;
+  const bool q8 = (fp8 & 1) != 0, qk8 = (fp8 & 2) != 0;
+  fp8 &= 1;
   std::vector<float> X(size_t(M) * D), Y(size_t(M) * D), QKV(size_t(M) * 3 * D), O(size_t(M) * D),
       tmp(size_t(M) * D), Hd(size_t(M) * F);
   oracle_patch_embed(pix, m->patch_w, m->patch_b, m->pos, X.data(), B, T, m->patch_dim, D, fp8);
@@ -318,6 +336,13 @@ void oracle_encode(const oracle_model* m, const float* pix, float* out, long B, 
   for (int l = 0; l < layers; ++l) {
     layernorm(X.data(), m->ln1_g[l], m->ln1_b[l], Y.data(), M, D, 1e-6f);
     linear(Y.data(), D, m->qkv_w[l], m->qkv_b[l], QKV.data(), M, 3 * D, D, q8);
+    if (qk8)  // Q and K columns of every row to E4M3 values
+      parallel(M, [&](long i) {
+        for (long c = 0; c < 2 * D; ++c) {
+          float& x = QKV[size_t(i * 3 * D + c)];
+          x = e4m3_value(16.0f * x) / 16.0f;
+        }
+      });
     parallel(B * H, [&](long bh) {
       const long b = bh / H, h = bh % H;
       const float* base = QKV.data() + b * T * 3 * D;

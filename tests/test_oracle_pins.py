@@ -283,3 +283,28 @@ def test_fp8_mode_quantises_both_gemm_operands():
     q = lambda a: torch.from_numpy((16 * a).astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy() / 16
     np.testing.assert_allclose(oracle.linear(A, W, fp8=True), q(A) @ q(W), rtol=1e-5, atol=1e-6)
     assert np.abs(oracle.linear(A, W, fp8=True) - A @ W).max() > 1e-3
+
+
+def test_fp8_attention_products_round_q_and_k_only():
+    """FP8 attention products ("FP8 attention and resident image/embedding transfers":
+    the QK product on E4M3 operands at scale 2^-4): the oracle's scores use
+    E4M3(16 q)/16 and E4M3(16 k)/16, rounded by torch's float8 cast here, while V and
+    the softmax stay exact; and the whole-network mode applies it to Q and K only."""
+    B, H, T, dh = 2, 2, 9, 72
+    q = synth.normal(15, 1, (B, T, H * dh)).astype(np.float64)
+    k = synth.normal(15, 2, (B, T, H * dh)).astype(np.float64)
+    v = synth.normal(15, 3, (B, T, H * dh)).astype(np.float64)
+    r8 = lambda a: torch.from_numpy((16 * a).astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy() / 16
+    want = oracle.attention(r8(q), r8(k), v, H, dh)
+    got = oracle.attention(q, k, v, H, dh, qk_fp8=True)
+    np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-6)
+    assert np.abs(got - oracle.attention(q, k, v, H, dh)).max() > 1e-4  # the rounding does change the scores
+    # V is not rounded: rounding it too gives a different result
+    assert np.abs(got - oracle.attention(r8(q), r8(k), r8(v), H, dh)).max() > 1e-4
+    # whole network: the mode only touches attention (same as unquantised with Q, K exact
+    # when the FP8 attention bit is off); with it on, the output moves but stays close
+    d = synth.vit_small(1)
+    m = oracle.OracleModel.from_synth(0, d)
+    pix = synth.pixels(1, 2, d.tokens, d.patch_dim)
+    base, qk = m.encode(pix), m.encode(pix, fp8_attention=True)
+    assert 0 < np.abs(base - qk).max() < 0.1
