@@ -8,6 +8,7 @@ tensor-core target is quoted in); weights are drawn by the seeded generator
 and resident in HBM; pixels are uniform in [-1, 1].
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--dtype f16|e4m3] [--unfused-qkv]
+                  [--fp8-attention]
   python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
 Prints one JSON line (rank 0). Multi-GPU runs (torchrun, one rank per GPU)
@@ -177,11 +178,13 @@ def run_reference(args, world, rank):
 
 
 def config(args, world):
-    return {"workload": f"27-layer So400m/14 @378px + MAP pooling, {args.dtype.upper()} GEMM operands, "
+    qk = ", E4M3 attention scores" if getattr(args, "fp8_attention", False) else ""
+    return {"workload": f"27-layer So400m/14 @378px + MAP pooling, {args.dtype.upper()} GEMM operands{qk}, "
                         f"batch {args.batch} per GPU",
             "global_batch": args.batch * world, "layers": L27, "tokens": T, "width": D,
             "gemm_dtype": args.dtype, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "qkv": "three GEMMs" if getattr(args, "unfused_qkv", False) else "one fused GEMM",
+            "attention_scores": "E4M3 Q, K" if getattr(args, "fp8_attention", False) else "F16 Q, K",
             "l2": "no flush: every step streams 0.85 GB of F16 weights and several GB of activations, "
                   "far above the 129 MB L2"}
 
@@ -194,6 +197,7 @@ def main():
     ap.add_argument("--batch", type=int, default=32, help="images per GPU per step")
     ap.add_argument("--dtype", choices=("f16", "e4m3"), default="f16")
     ap.add_argument("--unfused-qkv", action="store_true", help="Q, K, V as three GEMMs (comparison only)")
+    ap.add_argument("--fp8-attention", action="store_true", help="scores on E4M3 Q and K (FP8 attention products)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-layers", type=int, default=4, help="layers in the timed oracle sample")
@@ -230,7 +234,8 @@ def main():
     out = torch.empty(count, 1, D, dtype=torch.float16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    flags = vt.SV_ENCODE_UNFUSED_QKV if args.unfused_qkv else 0
+    flags = (vt.SV_ENCODE_UNFUSED_QKV if args.unfused_qkv else 0) | \
+        (vt.SV_ENCODE_FP8_ATTENTION if args.fp8_attention else 0)
 
     def step():
         vt.sv_encode_ex(pix, out, count, L27, gdt, flags, stream)

@@ -112,11 +112,21 @@ typedef enum {
    * weight instead of one 1152 -> 3456 GEMM (the pages' fused-QKV comparison:
    * "Fused QKV projection" section, which measured fusion as about 7.6% faster).
    * The results are the same; only the launch structure differs. */
-  SV_ENCODE_UNFUSED_QKV = 1
+  SV_ENCODE_UNFUSED_QKV = 1,
+  /* FP8 attention products ("FP8 attention and resident image/embedding
+   * transfers", Projected attention and Full 27-layer ViT): every encoder
+   * layer's scores S = Q K^T are computed on E4M3 operands at scale 2^-4
+   * (Q and K written as E4M3(16 x) by the QKV projection's epilogue, the
+   * producer-side quantisation those pages name as the profitable form).
+   * Softmax, the P V product (F16) and the output precision are unchanged; the
+   * MAP head's single-query attention is not affected. Combines with either
+   * gemm_dtype. */
+  SV_ENCODE_FP8_ATTENTION = 2
 } sv_encode_flags;
 
 /*
- * sv_encode with options: flags is 0 (exactly sv_encode) or SV_ENCODE_UNFUSED_QKV.
+ * sv_encode with options: flags is 0 (exactly sv_encode) or any OR of
+ * SV_ENCODE_UNFUSED_QKV and SV_ENCODE_FP8_ATTENTION.
  * Each (batch, gemm_dtype, flags) combination has its own cached workspace.
  * Errors: as sv_encode; unknown flag bits -> SV_ERR_INVALID_ARG.
  */
@@ -203,6 +213,22 @@ sv_status sv_ln_gemm(const void* x, const void* gamma, const void* beta, float e
  */
 sv_status sv_attention(const void* qkv, void* o, int batch, int heads, int tokens, int head_dim, float scale,
                        int out_dtype, void* stream);
+
+/* Options of sv_attention_ex. */
+typedef enum {
+  /* Scores on E4M3 operands: Q and K rounded to E4M3 at scale 2^-4 (stored as
+   * E4M3(16 x)) before S = Q K^T ("FP8 attention and resident image/embedding
+   * transfers", Projected attention); everything else as sv_attention. */
+  SV_ATTENTION_QK_E4M3 = 1
+} sv_attention_flags;
+
+/*
+ * sv_attention with options: flags is 0 (exactly sv_attention) or
+ * SV_ATTENTION_QK_E4M3. Errors: as sv_attention; unknown flag bits ->
+ * SV_ERR_INVALID_ARG.
+ */
+sv_status sv_attention_ex(const void* qkv, void* o, int batch, int heads, int tokens, int head_dim, float scale,
+                          int out_dtype, int flags, void* stream);
 
 /*
  * MAP pooling head with the resident weights ("SigLIP ViT benchmark":

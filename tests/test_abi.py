@@ -76,6 +76,8 @@ def test_errors_before_device_work(lib):
     # head width other than 72 is not implemented
     assert lib.sv_attention(p16, p16, 1, 2, 4, 64, 0.125, 0, None) == vt.SV_ERR_UNSUPPORTED
     assert lib.sv_attention(p16, p16, 0, 2, 4, 72, 0.125, 0, None) == vt.SV_ERR_INVALID_ARG
+    # unknown attention option bits
+    assert lib.sv_attention_ex(p16, p16, 1, 2, 4, 72, 0.125, 0, 2, None) == vt.SV_ERR_INVALID_ARG
     # quantiser length
     assert lib.sv_quantize_e4m3(p16, p16, 15, None) == vt.SV_ERR_INVALID_ARG
     # wait-probe limits

@@ -6,7 +6,8 @@ Configurations (the pages' workloads; weights and pixels from synth/):
   - one So400m/14 layer + MAP at batch 1 and batch 8, F16 GEMMs;
   - 27 layers + MAP at batch 1, F16 GEMMs;
   - 27 layers + MAP at batch 2 with E4M3 GEMM operands at scale 2^-4, against
-    the unquantised oracle (and the oracle's operand-rounding mode).
+    the unquantised oracle (and the oracle's operand-rounding mode), also with
+    the FP8 attention products (Q and K in E4M3).
 Tolerances are the stated ones: F16 one layer max-abs <= 2e-2 and cosine
 >= 0.9999; F16 27 layers cosine >= 0.995; E4M3 27 layers cosine >= 0.99 and
 max-abs <= 0.5 (cosine per image, minimum over images).
@@ -102,6 +103,29 @@ def test_unfused_qkv_matches_fused(sv, so400m, dtype):
         assert cosine_rows(b, ref).min() >= 0.9999
 
 
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_fp8_attention_two_layers(sv, so400m, dtype):
+    """FP8 attention products ("FP8 attention and resident image/embedding
+    transfers"): scores on E4M3 Q and K written by the QKV epilogue, against the
+    oracle's QK-rounding mode (one-layer tolerances for F16 GEMMs; the E4M3 GEMM
+    bound for E4M3 GEMMs), and still within the F16 bound of plain attention."""
+    B = 2
+    pix = synth.pixels(5, B)
+    x = torch.from_numpy(pix).cuda()
+    D = sv.sv_model_dims()["width"]
+    out = torch.empty(B, 1, D, dtype=torch.float16, device="cuda")
+    sv.sv_encode_ex(x, out, B, 2, dtype, sv.SV_ENCODE_FP8_ATTENTION)
+    sv.sv_sync()
+    got = host(out).reshape(B, -1)
+    ref_qk = so400m.encode(pix, layers=2, fp8=dtype == 1, fp8_attention=True)
+    if dtype == 0:
+        assert np.abs(got - ref_qk).max() <= 2e-2
+        assert cosine_rows(got, ref_qk).min() >= 0.9999
+    else:
+        assert cosine_rows(got, ref_qk).min() >= 0.995
+    assert cosine_rows(got, so400m.encode(pix, layers=2)).min() >= 0.99
+
+
 @pytest.fixture(scope="module")
 def ref27(so400m):
     pix = synth.pixels(1, 2)
@@ -120,3 +144,18 @@ def test_27_layers_e4m3_batch2(sv, ref27):
     assert cosine_rows(got, ref).min() >= 0.99
     assert np.abs(got - ref).max() <= 0.5
     assert cosine_rows(got, ref_q).min() >= 0.995
+
+
+def test_27_layers_e4m3_fp8_attention_batch2(sv, so400m, ref27):
+    """E4M3 GEMMs and FP8 attention products ("FP8 attention and resident
+    image/embedding transfers", Full 27-layer ViT: against the unquantised
+    reference, cosine > 0.99), plus the oracle with both roundings."""
+    pix, ref, _ = ref27
+    D = sv.sv_model_dims()["width"]
+    out = torch.empty(2, 1, D, dtype=torch.float16, device="cuda")
+    sv.sv_encode_ex(torch.from_numpy(pix).cuda(), out, 2, 27, 1, sv.SV_ENCODE_FP8_ATTENTION)
+    sv.sv_sync()
+    got = host(out).reshape(2, -1)
+    assert cosine_rows(got, ref).min() >= 0.99
+    assert np.abs(got - ref).max() <= 0.5
+    assert cosine_rows(got, so400m.encode(pix, fp8=True, fp8_attention=True)).min() >= 0.995

@@ -193,6 +193,27 @@ def test_attention(sv, B, H, T, sharp):
     assert_close(host(o), ref, RT, RT * vmax, f"attention B{B} H{H} T{T}")
 
 
+@pytest.mark.parametrize("B,H,T,sharp", [(1, 2, 4, 1.0), (2, 16, 729, 1.0), (1, 3, 200, 3.0), (3, 4, 300, 1.5),
+                                         (1, 1, 129, 1.0), (1, 2, 1, 1.0)])
+def test_attention_qk_e4m3(sv, B, H, T, sharp):
+    """FP8 score products ("FP8 attention and resident image/embedding transfers",
+    Projected attention): both sides round the same F16 Q and K values to E4M3 at
+    scale 2^-4, so the F16 attention tolerance holds against the oracle's QK-rounding
+    mode, while the unrounded attention is measurably further away."""
+    D = H * 72
+    qkv = synth.normal(180 + T, 1, (B, T, 3 * D))
+    qkv[..., :D] = (qkv[..., :D].astype(np.float32) * sharp).astype(np.float16)
+    o = torch.empty(B, T, D, dtype=torch.float16, device="cuda")
+    sv.sv_attention_ex(dev_f16(qkv), o, B, H, T, flags=sv.SV_ATTENTION_QK_E4M3)
+    sv.sv_sync()
+    ref = oracle.attention(qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:], H, 72, qk_fp8=True)
+    vmax = float(np.abs(qkv[..., 2 * D:].astype(np.float64)).max())
+    got = host(o)
+    assert_close(got, ref, RT, RT * vmax, f"attention qk-e4m3 B{B} H{H} T{T}")
+    if T >= 100:
+        assert np.abs(got - _attn_ref(qkv, H)).max() > 4 * RT * vmax
+
+
 def test_attention_e4m3_output_and_poisoned_neighbours(sv):
     """Rows past an image's last token and columns outside a head are never
     read as data: the qkv buffer sits inside NaN-filled memory and the output

@@ -38,6 +38,7 @@ SIGNATURES = [
     ("sv_ln_gemm", _I, [_VP, _VP, _VP, _F, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     ("sv_pack_patches", _I, [_VP, _VP, _I, _I, _I, _I, _VP]),
     ("sv_attention", _I, [_VP, _VP, _I, _I, _I, _I, _F, _I, _VP]),
+    ("sv_attention_ex", _I, [_VP, _VP, _I, _I, _I, _I, _F, _I, _I, _VP]),
     ("sv_map_pool", _I, [_VP, _VP, _I, _I, _VP]),
     ("sv_map_pool_static", _I, [_VP, _VP, _I, _I, _VP]),
     ("sv_quantize_e4m3", _I, [_VP, _VP, _SZ, _VP]),
@@ -115,6 +116,8 @@ def sv_model_dims() -> dict:
 
 
 SV_ENCODE_UNFUSED_QKV = 1
+SV_ENCODE_FP8_ATTENTION = 2
+SV_ATTENTION_QK_E4M3 = 1
 
 
 def sv_encode_ex(pixels, out, batch: int, layers: int, gemm_dtype: int = SV_GEMM_F16, flags: int = 0, stream=None):
@@ -154,6 +157,13 @@ def sv_attention(qkv, o, batch: int, heads: int, tokens: int, head_dim: int = 72
     s = head_dim ** -0.5 if scale is None else scale
     _check("sv_attention", load().sv_attention(_ptr(qkv), _ptr(o), batch, heads, tokens, head_dim, s, out_dtype,
                                                _stream(stream)))
+
+
+def sv_attention_ex(qkv, o, batch: int, heads: int, tokens: int, head_dim: int = 72, scale: float | None = None,
+                    out_dtype: int = 0, flags: int = 0, stream=None):
+    s = head_dim ** -0.5 if scale is None else scale
+    _check("sv_attention_ex", load().sv_attention_ex(_ptr(qkv), _ptr(o), batch, heads, tokens, head_dim, s,
+                                                     out_dtype, flags, _stream(stream)))
 
 
 def sv_map_pool(x, out, batch: int, gemm_dtype: int = SV_GEMM_F16, stream=None):

@@ -119,6 +119,7 @@ struct MapPlan {
 struct Plan {
   int B = 0, fp8 = 0;
   int qkv_calls = 1;     // GEMMs per layer for Q, K, V: 1 fused, or 3 (SV_ENCODE_UNFUSED_QKV)
+  int qk8 = 0;           // scores on E4M3 Q and K (SV_ENCODE_FP8_ATTENTION)
   bool fold_ln = false;  // LN1 / LN2 folded into the QKV / MLP-up GEMMs (F16 operands)
   void* mem = nullptr;
   size_t bytes = 0;
@@ -393,6 +394,7 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
   p->B = B;
   p->fp8 = fp8;
   p->qkv_calls = (flags & SV_ENCODE_UNFUSED_QKV) ? 3 : 1;
+  p->qk8 = (flags & SV_ENCODE_FP8_ATTENTION) ? 1 : 0;
   p->fold_ln = !fp8;
   Carver c{nullptr};
   for (int pass = 0; pass < 2; ++pass) {
@@ -455,6 +457,7 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
       qe.blk_H = d.H;
       qe.blk_B = B;
       qe.blk_col0 = int(r0);
+      qe.blk_qk8 = p->qk8;
       const void* wptr = fp8 ? static_cast<const void*>(w.qkv_w8 + r0 * d.D) : static_cast<const void*>(w.qkv_w + r0 * d.D);
       st = make_call(&p->qkv[i * size_t(nq) + size_t(j)], ln_in, wptr, Mi, wq, d.D, fp8, qe, d.D);
     }
@@ -535,8 +538,8 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
     for (int j = 0; j < p.qkv_calls; ++j) SV_TRY(run_gemm(p.qkv[i * size_t(p.qkv_calls) + size_t(j)], s));
     {
       Launch L(kKindAttn, 4.0 * B * d.H * double(d.T) * double(d.T) * 72.0,
-               double(M) * 3 * d.D * 2.0 + double(M) * d.D * (fp8 ? 1.0 : 2.0), s);
-      SV_TRY(attention_launch(p.QKV, p.O, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, s));
+               double(M) * d.D * (2 * (p.qk8 ? 1.0 : 2.0) + 2.0) + double(M) * d.D * (fp8 ? 1.0 : 2.0), s);
+      SV_TRY(attention_launch(p.QKV, p.O, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, p.qk8, s));
     }
     SV_TRY(run_gemm(p.out[i], s));
     SV_TRY(p.fold_ln ? run_ln_stats(p.X, p.ln_r, p.ln_aug, M, s) : run_ln(p.X, w.ln2_g, w.ln2_b, p.Y, M, fp8, s));
@@ -678,7 +681,7 @@ sv_status sv_encode_ex(const void* pixels, void* out, int batch, int layers, int
                        void* stream) {
   SV_TRY(check_ready());
   if (!pixels || !out || batch < 1 || layers < 1 || layers > g_w.d.L ||
-      (gemm_dtype != SV_GEMM_F16 && gemm_dtype != SV_GEMM_E4M3) || (flags & ~SV_ENCODE_UNFUSED_QKV)) {
+      (gemm_dtype != SV_GEMM_F16 && gemm_dtype != SV_GEMM_E4M3) || (flags & ~(SV_ENCODE_UNFUSED_QKV | SV_ENCODE_FP8_ATTENTION))) {
     set_error("sv_encode: bad arguments (batch %d, layers %d of %d, gemm_dtype %d, flags %d)", batch, layers,
               g_w.d.L, gemm_dtype, flags);
     return SV_ERR_INVALID_ARG;
@@ -822,8 +825,13 @@ sv_status sv_layernorm(const void* x, const void* gamma, const void* beta, void*
 
 sv_status sv_attention(const void* qkv, void* o, int batch, int heads, int tokens, int head_dim, float scale,
                        int out_dtype, void* stream) {
+  return sv_attention_ex(qkv, o, batch, heads, tokens, head_dim, scale, out_dtype, 0, stream);
+}
+
+sv_status sv_attention_ex(const void* qkv, void* o, int batch, int heads, int tokens, int head_dim, float scale,
+                          int out_dtype, int flags, void* stream) {
   if (!qkv || !o || batch < 1 || heads < 1 || tokens < 1 || batch > 65535 || !std::isfinite(scale) ||
-      (out_dtype != 0 && out_dtype != 1)) {
+      (out_dtype != 0 && out_dtype != 1) || (flags & ~SV_ATTENTION_QK_E4M3)) {
     set_error("sv_attention: bad arguments");
     return SV_ERR_INVALID_ARG;
   }
@@ -855,10 +863,12 @@ sv_status sv_attention(const void* qkv, void* o, int batch, int heads, int token
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   {
     Launch L(kKindOther, 0.0, double(batch) * tokens * 3 * heads * 72 * 4.0, s);
-    SV_TRY(attention_repack_launch(static_cast<const __half*>(qkv), g_attn_scratch, batch, tokens, heads, s));
+    SV_TRY(attention_repack_launch(static_cast<const __half*>(qkv), g_attn_scratch, batch, tokens, heads,
+                                   flags & SV_ATTENTION_QK_E4M3, s));
   }
   Launch L(kKindAttn, 4.0 * batch * heads * double(tokens) * tokens * 72.0, 0.0, s);
-  return attention_launch(g_attn_scratch, o, batch, tokens, heads, scale, out_dtype, s);
+  return attention_launch(g_attn_scratch, o, batch, tokens, heads, scale, out_dtype, flags & SV_ATTENTION_QK_E4M3,
+                          s);
 }
 
 sv_status sv_map_pool(const void* x, void* out, int batch, int gemm_dtype, void* stream) {

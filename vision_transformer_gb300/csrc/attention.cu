@@ -13,6 +13,13 @@
 // (column group of 8, then row, then 8 values), so a tile arrives with one
 // bulk copy.
 //
+// FP8 score products ("FP8 attention and resident image/embedding transfers",
+// Projected attention: the QK product on E4M3 operands at scale 2^-4, both
+// operands written quantised by their producer): Q and K blocks hold E4M3(16 x)
+// in 16-value groups (10 KB a tile), S = Q K^T runs as three kind::f8f6f4 MMAs
+// of K = 32 (72 columns padded to 96) and the softmax scale absorbs the 2^-8;
+// P V stays F16 (P reaches 2^15, beyond E4M3's range).
+//
 // Padding contract ("SigLIP optimized execution and PV padding", cause and
 // fix: padding columns were once read as data and turned outputs into NaN):
 //   - head width 72 is padded to 80 for the MMA K / N steps: the pad column
@@ -52,17 +59,22 @@ constexpr int kTile = 128;                   // queries per group, keys per step
 constexpr int kGroupBytes = kTile * 16;      // 2048: one column group of a tile
 constexpr int kBlockBytes = kGroups * kGroupBytes;  // 18432: one operand tile in memory
 constexpr int kOpBytes = 10 * kGroupBytes;   // 80 columns in shared memory (72 + zero pad)
+// E4M3 Q / K tiles (FP8 score products): 5 groups of 16 values in memory (72 columns and
+// 8 zero bytes), 6 in shared memory (96 columns: three MMA K steps of 32)
+constexpr int kGroups8 = 5;
+constexpr int kOpBytes8 = 6 * kGroupBytes;
 constexpr int kPBytes = 16 * kGroupBytes;    // 128 keys of probabilities
 constexpr int kThreads = 352;
 constexpr int kBarBytes = 384;  // barriers, TMEM address slot, abort flag
 
 // Shared memory map (offsets from the 1024-aligned base) for QB query buffers
-// (of two tiles each), KS key stages and VS value stages.
-template <int QB, int KS, int VS>
+// (of two tiles each), KS key stages and VS value stages; QK8: E4M3 Q and K tiles.
+template <int QB, int KS, int VS, bool QK8>
 struct Smem {
+  static constexpr int kQKOp = QK8 ? kOpBytes8 : kOpBytes;  // one Q or K tile
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * QB * kOpBytes;
-  static constexpr int kOffV = kOffK + KS * kOpBytes;
+  static constexpr int kOffK = kOffQ + 2 * QB * kQKOp;
+  static constexpr int kOffV = kOffK + KS * kQKOp;
   static constexpr int kOffP = kOffV + VS * kOpBytes;  // one buffer per softmax group
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
   static constexpr int kBytes = 1024 + kOffBar + kBarBytes;
@@ -122,14 +134,16 @@ __device__ __forceinline__ int tile_rows(int T, int tile) {
   return v <= 0 ? 0 : (v < kTile ? v : kTile);
 }
 
-// Copies the existing rows of one operand tile; returns the bytes it will deliver.
-__device__ __forceinline__ uint32_t copy_tile(uint32_t dst, const uint8_t* src, int rows, uint32_t bar) {
+// Copies the existing rows of the first `groups` column groups of one operand tile;
+// returns the bytes it will deliver.
+__device__ __forceinline__ uint32_t copy_tile(uint32_t dst, const uint8_t* src, int rows, uint32_t bar,
+                                              int groups) {
   if (rows == kTile) {
-    bulk_copy(dst, src, kBlockBytes, bar);
-    return kBlockBytes;
+    bulk_copy(dst, src, uint32_t(groups * kGroupBytes), bar);
+    return uint32_t(groups * kGroupBytes);
   }
-  for (int g = 0; g < kGroups; ++g) bulk_copy(dst + g * kGroupBytes, src + g * kGroupBytes, rows * 16, bar);
-  return uint32_t(kGroups * rows * 16);
+  for (int g = 0; g < groups; ++g) bulk_copy(dst + g * kGroupBytes, src + g * kGroupBytes, rows * 16, bar);
+  return uint32_t(groups * rows * 16);
 }
 
 // As copy_tile, and the rows past the last token are filled with zeros (a V tile:
@@ -147,8 +161,8 @@ __device__ __forceinline__ uint32_t copy_tile_zero_tail(uint32_t dst, const uint
   return kBlockBytes;
 }
 
-__device__ __forceinline__ uint32_t tile_bytes(int rows) {
-  return rows == kTile ? uint32_t(kBlockBytes) : uint32_t(kGroups * rows * 16);
+__device__ __forceinline__ uint32_t tile_bytes(int rows, int groups) {
+  return uint32_t(groups * (rows == kTile ? kGroupBytes : rows * 16));
 }
 
 // Work item -> (query pair, head, image); the query pairs of one (image, head)
@@ -168,11 +182,12 @@ __device__ __forceinline__ Item item_of(int it, int nq, int H) {
 // Persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...
 // The K / V stream and the softmax pipeline run on across item boundaries; Q is
 // double buffered so the next item's queries arrive during the current item.
-template <int QB, int KS, int VS>
+template <int QB, int KS, int VS, bool QK8>
 // 11 warps: three share each of three SM sub-partitions, so a thread may hold at most
 // 16384 / (3 x 32) registers, rounded down to the allocation granule.
 __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtensorMap tm_out, const Params p) {
-  using L = Smem<QB, KS, VS>;
+  using L = Smem<QB, KS, VS, QK8>;
+  constexpr int kQKOp = L::kQKOp, kQKGroups = QK8 ? kGroups8 : kGroups;
   constexpr int kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffP = L::kOffP, kOffBar = L::kOffBar;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -257,11 +272,13 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
         const uint32_t qph = (n / QB) & 1;
         if (!mbar_wait(bar(kBarQEmpty + qb), qph ^ 1, abort_flag, p.err)) break;
         const int qr0 = tile_rows(T, 2 * I.qp), qr1 = tile_rows(T, 2 * I.qp + 1);
-        mbar_arrive_expect_tx(bar(kBarQFull + qb), tile_bytes(qr0) + (qr1 ? tile_bytes(qr1) : 0));
-        copy_tile(sbase + kOffQ + (2 * qb) * kOpBytes, block(0, I.b, I.h, 2 * I.qp), qr0, bar(kBarQFull + qb));
+        mbar_arrive_expect_tx(bar(kBarQFull + qb),
+                              tile_bytes(qr0, kQKGroups) + (qr1 ? tile_bytes(qr1, kQKGroups) : 0));
+        copy_tile(sbase + kOffQ + (2 * qb) * kQKOp, block(0, I.b, I.h, 2 * I.qp), qr0, bar(kBarQFull + qb),
+                  kQKGroups);
         if (qr1)
-          copy_tile(sbase + kOffQ + (2 * qb + 1) * kOpBytes, block(0, I.b, I.h, 2 * I.qp + 1), qr1,
-                    bar(kBarQFull + qb));
+          copy_tile(sbase + kOffQ + (2 * qb + 1) * kQKOp, block(0, I.b, I.h, 2 * I.qp + 1), qr1,
+                    bar(kBarQFull + qb), kQKGroups);
         note(qb, qph);
         for (int j = 0; j < nkv; ++j) {
           const int t = n * nkv + j, ks = t % KS, vs = t % VS;
@@ -271,8 +288,8 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(kBarKFull + ks), tile_bytes(rows));
-          copy_tile(sbase + kOffK + ks * kOpBytes, block(1, I.b, I.h, j), rows, bar(kBarKFull + ks));
+          mbar_arrive_expect_tx(bar(kBarKFull + ks), tile_bytes(rows, kQKGroups));
+          copy_tile(sbase + kOffK + ks * kQKOp, block(1, I.b, I.h, j), rows, bar(kBarKFull + ks), kQKGroups);
           note(4 + ks, kph);
           if (!mbar_wait(bar(kBarVEmpty + vs), vph ^ 1, abort_flag, p.err)) {
             ok = false;
@@ -297,7 +314,8 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
       // each 64-key half of P(t) once that half is written, V_t is in and (an item's
       // first tile) the group has read the previous item's O.
       const int w = warp - 1;
-      constexpr uint32_t idesc_s = make_idesc(128, 128, 0, false);  // S = Q K^T, both K-major
+      // S = Q K^T, both K-major (F16, or E4M3 with the same type code 0 under kind::f8f6f4)
+      constexpr uint32_t idesc_s = make_idesc(128, 128, 0, false);
       constexpr uint32_t idesc_o = make_idesc(128, 80, 0, true);    // O = P V, V MN-major
       auto issue_s = [&](int t) -> bool {
         const int n = t / nkv, j = t - n * nkv;
@@ -305,11 +323,18 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
         if (!mbar_wait(bar(kBarSEmpty + w), (t & 1) ^ 1, abort_flag, p.err)) return false;
         if (j == 0 && !mbar_wait(bar(kBarQFull + n % QB), (n / QB) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
-        const uint32_t qa = sbase + kOffQ + (2 * (n % QB) + w) * kOpBytes, ka = sbase + kOffK + (t % KS) * kOpBytes;
+        const uint32_t qa = sbase + kOffQ + (2 * (n % QB) + w) * kQKOp, ka = sbase + kOffK + (t % KS) * kQKOp;
+        if (QK8) {
 #pragma unroll
-        for (int kk = 0; kk < 5; ++kk)  // K = 80 in steps of 16 (two column groups)
-          mma_f16(tmem + uint32_t(w * 128), make_sdesc(qa + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
-                  make_sdesc(ka + kk * 2 * kGroupBytes, kGroupBytes, 128, 0), idesc_s, kk > 0);
+          for (int kk = 0; kk < 3; ++kk)  // K = 96 in steps of 32 (two 16-byte column groups)
+            mma_f8(tmem + uint32_t(w * 128), make_sdesc(qa + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
+                   make_sdesc(ka + kk * 2 * kGroupBytes, kGroupBytes, 128, 0), idesc_s, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 5; ++kk)  // K = 80 in steps of 16 (two column groups)
+            mma_f16(tmem + uint32_t(w * 128), make_sdesc(qa + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
+                    make_sdesc(ka + kk * 2 * kGroupBytes, kGroupBytes, 128, 0), idesc_s, kk > 0);
+        }
         tc_commit(bar(kBarSFull + w));
         tc_commit(bar(kBarKEmpty + t % KS));
         if (j == nkv - 1) tc_commit(bar(kBarQEmpty + n % QB));
@@ -349,7 +374,7 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
     const uint32_t s_tm = tmem + uint32_t(w * 128) + lane_off;
     const uint32_t o_tm = tmem + uint32_t(256 + w * 128) + lane_off;
     uint8_t* pbuf = smem + kOffP + w * kPBytes;
-    const float sl2 = p.scale_log2;
+    const float sl2 = QK8 ? p.scale_log2 * (1.0f / 256.0f) : p.scale_log2;  // E4M3 operands hold 16 q, 16 k
     const int D = p.H * kDh;
     // An item's output rows: the final O (with its row sum in column 72) of the group's
     // query tile, read from TMEM, scaled by 1 / row sum. F16 rows are staged as this
@@ -558,8 +583,10 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
 }
 
 // Row-major [B, T, 3 D] -> head-blocked; one thread per 16-byte group of 8 values.
+// qk8: Q and K as E4M3(16 x), 8 bytes per group (the head's last group also writes the
+// zero pad of its 16-value group).
 __global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restrict__ blk, int B, int T, int H,
-                              int tiles) {
+                              int tiles, int qk8) {
   const int D = H * kDh;
   const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
   const long per_row = 3L * D / 8;
@@ -569,8 +596,25 @@ __global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restric
   const int bimg = int(m / T), t = int(m - long(bimg) * T);
   const int which = col / D, rem = col - which * D, h = rem / kDh, cg = (rem - h * kDh) >> 3;
   const size_t idx = ((size_t(which) * B + bimg) * H + h) * tiles + (t >> 7);
-  *reinterpret_cast<uint4*>(blk + (idx * kGroups + cg) * kGroupBytes + (t & 127) * 16) =
-      *reinterpret_cast<const uint4*>(qkv + m * 3 * D + col);
+  const uint4 u = *reinterpret_cast<const uint4*>(qkv + m * 3 * D + col);
+  uint8_t* dst = blk + idx * kBlockBytes + (t & 127) * 16;
+  if (qk8 && which < 2) {
+    const __half2* hv = reinterpret_cast<const __half2*>(&u);
+    uint2 w8;
+    __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&w8);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(hv[i]);
+      q[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * f.x, 16.0f * f.y), __NV_SATFINITE, __NV_E4M3);
+    }
+    uint8_t* d8 = dst + (cg >> 1) * kGroupBytes + (cg & 1) * 8;
+    if (cg == kGroups - 1)
+      *reinterpret_cast<uint4*>(d8) = make_uint4(w8.x, w8.y, 0u, 0u);
+    else
+      *reinterpret_cast<uint2*>(d8) = w8;
+    return;
+  }
+  *reinterpret_cast<uint4*>(dst + cg * kGroupBytes) = u;
 }
 
 // Buffer configuration: 0 = two Q buffers, 2 + 2 K / V stages; 1 = one Q buffer,
@@ -579,16 +623,17 @@ __global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restric
 int g_attention_config = 1;
 int attention_config() { return g_attention_config; }
 
-template <int QB, int KS, int VS>
+template <int QB, int KS, int VS, bool QK8>
 sv_status attention_launch_cfg(const CUtensorMap& tmo, const Params& p, int grid, cudaStream_t s) {
   static bool attr_set = false;
-  auto kern = attention_kernel<QB, KS, VS>;
+  using L = Smem<QB, KS, VS, QK8>;
+  auto kern = attention_kernel<QB, KS, VS, QK8>;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<QB, KS, VS>::kBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
     attr_set = true;
   }
-  kern<<<unsigned(grid), kThreads, Smem<QB, KS, VS>::kBytes, s>>>(tmo, p);
+  kern<<<unsigned(grid), kThreads, L::kBytes, s>>>(tmo, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return SV_OK;
@@ -600,15 +645,15 @@ size_t attention_blocked_bytes(int B, int T, int H) {
   return size_t(3) * B * H * ((T + kTile - 1) / kTile) * size_t(kBlockBytes);
 }
 
-sv_status attention_repack_launch(const __half* qkv, void* blocked, int B, int T, int H, cudaStream_t s) {
+sv_status attention_repack_launch(const __half* qkv, void* blocked, int B, int T, int H, int qk8, cudaStream_t s) {
   const long n = long(B) * T * (3L * H * kDh / 8);
   repack_kernel<<<unsigned((n + 255) / 256), 256, 0, s>>>(qkv, static_cast<uint8_t*>(blocked), B, T, H,
-                                                           (T + kTile - 1) / kTile);
+                                                           (T + kTile - 1) / kTile, qk8);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "attention repack launch");
 }
 
-sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, float scale, int out_e4m3,
+sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, float scale, int out_e4m3, int qk8,
                            cudaStream_t s) {
   Params p;
   p.blocked = static_cast<const uint8_t*>(blocked);
@@ -634,10 +679,11 @@ sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, fl
     sv_status st = make_tmap(&tmo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, o, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != SV_OK) return st;
   }
+  if (qk8) return attention_launch_cfg<1, 3, 3, true>(tmo, p, grid, s);
   switch (attention_config()) {
-    case 1: return attention_launch_cfg<1, 3, 3>(tmo, p, grid, s);
-    case 2: return attention_launch_cfg<1, 4, 2>(tmo, p, grid, s);
-    default: return attention_launch_cfg<2, 2, 2>(tmo, p, grid, s);
+    case 1: return attention_launch_cfg<1, 3, 3, false>(tmo, p, grid, s);
+    case 2: return attention_launch_cfg<1, 4, 2, false>(tmo, p, grid, s);
+    default: return attention_launch_cfg<2, 2, 2, false>(tmo, p, grid, s);
   }
 }
 

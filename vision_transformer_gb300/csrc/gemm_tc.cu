@@ -85,6 +85,7 @@ struct Params {
   uint8_t* blk;
   int blk_T, blk_H, blk_B, blk_tiles;
   int blk_col0;  // first column of the fused [Q | K | V] space this GEMM's columns start at
+  int blk_qk8;   // Q and K as E4M3 (16 x value): 16-byte groups of 16 columns per row
 };
 
 // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), with
@@ -505,12 +506,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rem = col - which * D;
                 const int h = (rem * 58255) >> 22;  // rem / 72, exact for rem < 4096
                 const int cg = (rem - h * 72) >> 3;
+                uint8_t* dst = p.blk + which * which_stride + rowoff + size_t(h) * p.blk_tiles * 18432;
+                if (p.blk_qk8 && which < 2) {
+                  // E4M3 Q / K: column group cg is half of the 16-column group cg / 2;
+                  // the head's last group (columns 64..71) also writes the zero pad 72..79
+                  uint2 w8;
+                  __nv_fp8x2_storage_t* qq = reinterpret_cast<__nv_fp8x2_storage_t*>(&w8);
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    qq[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * v[8 * g + 2 * i], 16.0f * v[8 * g + 2 * i + 1]),
+                                                     __NV_SATFINITE, __NV_E4M3);
+                  uint8_t* d8 = dst + (cg >> 1) * 2048 + (cg & 1) * 8;
+                  if (cg == 8)
+                    *reinterpret_cast<uint4*>(d8) = make_uint4(w8.x, w8.y, 0u, 0u);
+                  else
+                    *reinterpret_cast<uint2*>(d8) = w8;
+                  continue;
+                }
                 uint4 w;
                 __half2* hh = reinterpret_cast<__half2*>(&w);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) hh[i] = __floats2half2_rn(v[8 * g + 2 * i], v[8 * g + 2 * i + 1]);
-                *reinterpret_cast<uint4*>(p.blk + which * which_stride + rowoff +
-                                          size_t(h) * p.blk_tiles * 18432 + cg * 2048) = w;
+                *reinterpret_cast<uint4*>(dst + cg * 2048) = w;
               }
           }
           continue;
@@ -806,6 +823,7 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.blk_H = e.blk_H;
   p.blk_B = e.blk_B;
   p.blk_col0 = e.blk_col0;
+  p.blk_qk8 = e.blk_qk8;
   p.blk_tiles = (e.blk_T + 127) / 128;
   p.act = e.act;
   p.out_e4m3 = e.out_e4m3;

@@ -46,6 +46,7 @@ struct GemmEpi {
   void* blk_out = nullptr;
   int blk_T = 0, blk_H = 0, blk_B = 0;
   int blk_col0 = 0;  // this GEMM's column 0 is column blk_col0 of the fused [Q | K | V] output
+  int blk_qk8 = 0;   // Q and K written as E4M3 (value x 16) in their blocks, for FP8 score products
   // LayerNorm of A folded in (A is the LayerNorm input, W already scaled by gamma):
   // the GEMM runs one more K block of 16, ln_aug_a [M, 16] . ln_aug_w [N, 16]^T =
   // -mean_m s_n, and the epilogue scales row m by ln_r[m] before adding `bias` (b').
@@ -90,11 +91,14 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s);
 // (which 0 = Q, 1 = K, 2 = V; tiles of 128 tokens), each block 9 column groups x 128 rows x
 // 8 f16 (2048 bytes per group: row r of group cg at cg*2048 + r*16). Rows past the last
 // token of an image are never written or read as data.
+// E4M3 Q / K (qk8, FP8 score products): the same block positions, each using its first
+// 5 groups of 128 rows x 16 values E4M3(16 x) (row r of group g at g*2048 + r*16; group 4
+// holds columns 64..71 and eight zero bytes).
 size_t attention_blocked_bytes(int B, int T, int H);
-// Row-major [B, T, 3*H*72] f16 -> head-blocked.
-sv_status attention_repack_launch(const __half* qkv, void* blocked, int B, int T, int H, cudaStream_t s);
-// o: [B, T, H*72] f16 / e4m3.
-sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, float scale, int out_e4m3,
+// Row-major [B, T, 3*H*72] f16 -> head-blocked (qk8: Q and K quantised to E4M3).
+sv_status attention_repack_launch(const __half* qkv, void* blocked, int B, int T, int H, int qk8, cudaStream_t s);
+// o: [B, T, H*72] f16 / e4m3. qk8: Q and K blocks are E4M3, S = Q K^T on E4M3 operands.
+sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, float scale, int out_e4m3, int qk8,
                            cudaStream_t s);
 
 // ---- elementwise (elementwise.cu)
