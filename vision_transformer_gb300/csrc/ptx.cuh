@@ -37,21 +37,33 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// kSleepNs > 0: a thread whose phase is not complete yet may be suspended for up
+// to that long (it resumes when the phase completes), instead of returning at
+// once to poll again; waiters that would otherwise spin for a long time then take
+// no issue slots or shared-memory cycles from the warps doing the work.
+template <uint32_t kSleepNs = 0>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kSleepNs == 0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kSleepNs)
+        : "memory");
+  }
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete. Gives up after
-// limit_ns of %globaltimer, or as soon as another thread of the CTA has given
-// up (*abort != 0): then sets *abort and the device error word, returns false.
 // Non-blocking test: has the phase with this parity completed?
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -65,13 +77,17 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Waits for the phase with the given parity to complete. Gives up after
+// limit_ns of %globaltimer, or as soon as another thread of the CTA has given
+// up (*abort != 0): then sets *abort and the device error word, returns false.
+template <uint32_t kSleepNs = 0>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* dev_err,
                                           unsigned long long limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kSleepNs>(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
+    if (mbar_try_wait<kSleepNs>(bar, parity)) return true;
+    if ((i & (kSleepNs ? 15u : 255u)) == 0) {
       if (*abort) return false;
       if (globaltimer() - t0 > limit_ns) {
         *abort = 1;
