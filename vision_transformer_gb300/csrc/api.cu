@@ -128,6 +128,7 @@ struct Plan {
   void* Y = nullptr;       // [M, D] LayerNorm output (GEMM operand)
   float* ln_r = nullptr;    // [M] 1/std of each row (F16 path: LayerNorm folded into the GEMMs)
   __half* ln_aug = nullptr;  // [M, 16] the folded GEMMs' extra K block (-mean)
+  float2* ln_part = nullptr;  // [M, kMaxLnTiles] per-tile row statistics from the GEMMs that write X
   __half* QKV = nullptr;  // head-blocked Q/K/V for attention; the MAP KV projection reuses it row-major
   void* O = nullptr;      // [M, D] attention output (GEMM operand)
   void* Hh = nullptr;     // [M, F] GELU output (GEMM operand)
@@ -403,6 +404,7 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
     p->Y = c.take(M * d.D * eb);
     p->ln_r = static_cast<float*>(c.take(M * sizeof(float)));
     p->ln_aug = static_cast<__half*>(c.take(M * 16 * sizeof(__half)));
+    p->ln_part = static_cast<float2*>(c.take(M * kMaxLnTiles * sizeof(float2)));
     const size_t qkv_bytes = attention_blocked_bytes(B, d.T, d.H);
     p->QKV = static_cast<__half*>(c.take(qkv_bytes > M * 3 * d.D * 2 ? qkv_bytes : M * 3 * d.D * 2));
     p->O = c.take(M * d.D * eb);
@@ -423,6 +425,8 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
   GemmEpi pe = epi(g_w.patch_b, p->X, sc);
   pe.pos = g_w.pos;
   pe.pos_rows = d.T;
+  // F16: the GEMMs that write X also write its row statistics for the next LayerNorm
+  if (p->fold_ln) pe.ln_part = p->ln_part;
   if ((st = make_call(&p->patch, p->A0, fp8 ? (const void*)g_w.patch_w8 : g_w.patch_w, Mi, d.D, d.Kp, fp8, pe, d.P)))
     return fail(st);
   p->qkv.resize(size_t(d.L) * size_t(p->qkv_calls));
@@ -461,12 +465,13 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
       const void* wptr = fp8 ? static_cast<const void*>(w.qkv_w8 + r0 * d.D) : static_cast<const void*>(w.qkv_w + r0 * d.D);
       st = make_call(&p->qkv[i * size_t(nq) + size_t(j)], ln_in, wptr, Mi, wq, d.D, fp8, qe, d.D);
     }
+    GemmEpi oe = epi(w.out_b, p->X, sc, SV_ACT_NONE, 0, p->X);
+    GemmEpi de = epi(w.fc2_b, p->X, sc, SV_ACT_NONE, 0, p->X);
+    if (p->fold_ln) oe.ln_part = de.ln_part = p->ln_part;
     if (st ||
-        (st = make_call(&p->out[i], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8,
-                        epi(w.out_b, p->X, sc, SV_ACT_NONE, 0, p->X), d.D)) ||
+        (st = make_call(&p->out[i], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8, oe, d.D)) ||
         (st = make_call(&p->fc1[i], ln_in, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8, fe, d.D)) ||
-        (st = make_call(&p->fc2[i], p->Hh, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, Mi, d.D, d.F, fp8,
-                        epi(w.fc2_b, p->X, sc, SV_ACT_NONE, 0, p->X), d.F)))
+        (st = make_call(&p->fc2[i], p->Hh, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, Mi, d.D, d.F, fp8, de, d.F)))
       return fail(st);
   }
   *out = p.get();
@@ -488,10 +493,11 @@ sv_status run_gemm(const GemmCall& c, cudaStream_t s) {
   return gemm_launch(c.g, c.e, s);
 }
 
-sv_status run_ln_stats(const __half* x, float* r, __half* aug, int rows, cudaStream_t s) {
-  const int D = g_w.d.D;
-  Launch L(kKindLN, 4.0 * rows * D, double(rows) * (D * 2.0 + 36.0), s);
-  return ln_stats_launch(x, r, aug, rows, D, 1e-6f, s);
+// LayerNorm statistics of X from the row statistics its producing GEMM wrote.
+sv_status run_ln_finalize(const Plan& p, const GemmCall& producer, int rows, cudaStream_t s) {
+  const int D = g_w.d.D, tiles = (D + producer.g.bn - 1) / producer.g.bn;
+  Launch L(kKindLN, 8.0 * rows * tiles, double(rows) * (tiles * 8.0 + 36.0), s);
+  return ln_finalize_launch(p.ln_part, tiles, producer.g.bn, p.ln_r, p.ln_aug, rows, D, 1e-6f, s);
 }
 
 sv_status run_ln(const __half* x, const __half* gm, const __half* bt, void* y, int rows, int out_e4m3,
@@ -534,7 +540,8 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
   for (int l = 0; l < layers; ++l) {
     const LayerW& w = g_w.layers[size_t(l)];
     const size_t i = size_t(l);
-    SV_TRY(p.fold_ln ? run_ln_stats(p.X, p.ln_r, p.ln_aug, M, s) : run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
+    SV_TRY(p.fold_ln ? run_ln_finalize(p, l == 0 ? p.patch : p.fc2[i - 1], M, s)
+                     : run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
     for (int j = 0; j < p.qkv_calls; ++j) SV_TRY(run_gemm(p.qkv[i * size_t(p.qkv_calls) + size_t(j)], s));
     {
       Launch L(kKindAttn, 4.0 * B * d.H * double(d.T) * double(d.T) * 72.0,
@@ -542,7 +549,7 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
       SV_TRY(attention_launch(p.QKV, p.O, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, p.qk8, s));
     }
     SV_TRY(run_gemm(p.out[i], s));
-    SV_TRY(p.fold_ln ? run_ln_stats(p.X, p.ln_r, p.ln_aug, M, s) : run_ln(p.X, w.ln2_g, w.ln2_b, p.Y, M, fp8, s));
+    SV_TRY(p.fold_ln ? run_ln_finalize(p, p.out[i], M, s) : run_ln(p.X, w.ln2_g, w.ln2_b, p.Y, M, fp8, s));
     SV_TRY(run_gemm(p.fc1[i], s));
     SV_TRY(run_gemm(p.fc2[i], s));
   }

@@ -295,6 +295,49 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, int* err) {
   }
 }
 
+// LayerNorm statistics from a GEMM epilogue's per-tile partials, one thread per row:
+// each tile has two partials, over its 32-column chunks c = 0, 2, ... and c = 1, 3, ...
+// (a partial covering no column is absent). Their (count, mean, M2) are merged left to
+// right with the pairwise update of
+// Chan, Golub and LeVeque (1979): n = na + nb, d = mean_b - mean_a,
+// mean = mean_a + d nb / n, M2 = M2a + M2b + d^2 na nb / n; then var = M2 / width
+// (biased, as the LayerNorm kernel) and the same r / aug outputs as its statistics mode.
+__global__ void __launch_bounds__(256) ln_finalize_kernel(const float2* __restrict__ part, int tiles, int tile_w,
+                                                         float* __restrict__ r, __half* __restrict__ aug,
+                                                         int rows, int width, float eps) {
+  const int row = int(blockIdx.x) * 256 + int(threadIdx.x);
+  if (row >= rows) return;
+  const float2* pr = part + size_t(row) * size_t(2 * tiles);
+  float n = 0.0f, mean = 0.0f, m2 = 0.0f;
+  for (int t = 0; t < tiles; ++t) {
+    const int w = min(tile_w, width - t * tile_w), chunks = (w + 31) / 32;
+    for (int h = 0; h < 2; ++h) {
+      int cols = 0;
+      for (int c = h; c < chunks; c += 2) cols += min(32, w - 32 * c);
+      if (cols == 0) continue;
+      const float nb = float(cols);
+      const float2 q = __ldg(pr + 2 * t + h);
+      const float nn = n + nb, d = q.x - mean;
+      mean = fmaf(d, nb / nn, mean);
+      m2 += q.y + d * d * (n * nb / nn);
+      n = nn;
+    }
+  }
+  const float rstd = rsqrtf(m2 / float(width) + eps);
+  const __half hi = __float2half_rn(-mean);
+  const __half lo = __float2half_rn(-mean - __half2float(hi));
+  const __half2 z = __float2half2_rn(0.0f);
+  uint4 w;
+  __half2* h = reinterpret_cast<__half2*>(&w);
+  h[0] = __halves2half2(hi, hi);
+  h[1] = __halves2half2(lo, __float2half_rn(0.0f));
+  h[2] = h[3] = z;
+  uint4* dst = reinterpret_cast<uint4*>(aug + size_t(row) * 16);
+  dst[0] = w;
+  dst[1] = make_uint4(0u, 0u, 0u, 0u);
+  r[row] = rstd;
+}
+
 // LayerNorm folded into the linear map that consumes it: with y = (x - mu) r . g + be
 // (r = 1/sqrt(var + eps)), y . W_n + b_n = r (x . W'_n - mu s_n) + b'_n where
 // W'_nk = g_k W_nk (rounded to F16, in place), s_n = sum_k W'_nk and
@@ -369,6 +412,13 @@ sv_status layernorm_launch(const __half* x, const __half* g, const __half* b, vo
 sv_status ln_stats_launch(const __half* x, float* stats_r, __half* stats_aug, int rows, int width, float eps,
                           cudaStream_t s) {
   return ln_any(x, nullptr, nullptr, nullptr, rows, width, eps, 0, stats_r, stats_aug, s);
+}
+
+sv_status ln_finalize_launch(const float2* part, int tiles, int tile_w, float* r, __half* aug, int rows, int width,
+                             float eps, cudaStream_t s) {
+  ln_finalize_kernel<<<unsigned((rows + 255) / 256), 256, 0, s>>>(part, tiles, tile_w, r, aug, rows, width, eps);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "ln_finalize launch");
 }
 
 sv_status fold_ln_launch(__half* W, const __half* g, const __half* be, const __half* b, __half* w_aug, __half* b_out,

@@ -37,7 +37,11 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBKBytes = 128;  // K bytes per stage: one 128-byte swizzle row
-constexpr int kThreads = 192;
+// Warp 0 loads, warp 1 issues the MMAs, warps 2 .. 9 run the epilogue: two per
+// TMEM lane quarter, each taking every other 32-column chunk of a tile (with four,
+// the epilogue of a K = 1152 tile took about as long as its main loop).
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 // Widest output tile used with CTA pairs (its TMEM: 2 x BN columns per CTA).
 constexpr int kPairMaxBn = 256;
 // Suspend limits (ns) of the mbarrier waits of each role. A waiter that polls
@@ -57,18 +61,18 @@ struct Cfg {
   static constexpr int kStageA = kBM * kBKBytes;
   static constexpr int kStageB = (PAIR ? BN / 2 : BN) * kBKBytes;
   static constexpr int kStage = kStageA + kStageB;
-  // epilogue staging: per epilogue warp a ring of four 32 x 32 blocks (residual in,
+  // epilogue staging: per epilogue warp a ring of two 32 x 32 blocks (residual in,
   // result out)
   static constexpr int kEpiBlock = 2048;
-  static constexpr int kEpiRing = 4;
-  static constexpr int kEpiBytes = 4 * kEpiRing * kEpiBlock;
+  static constexpr int kEpiRing = 2;
+  static constexpr int kEpiBytes = kEpiWarps * kEpiRing * kEpiBlock;
   static constexpr int kBarBytes = 320;
   static constexpr int kBudget = 232448 - 1024 - kEpiBytes - kBarBytes;
   static constexpr int kStages = kBudget / kStage < 8 ? kBudget / kStage : 8;
   static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
   static constexpr int kSmem = 1024 + kStages * kStage + kEpiBytes + kBarBytes;
   static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
-  static_assert(8 * (2 * kStages + 5 + 4 * kEpiRing) + 8 <= kBarBytes, "barrier area");
+  static_assert(8 * (2 * kStages + 5 + kEpiWarps * kEpiRing) + 8 <= kBarBytes, "barrier area");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
@@ -94,17 +98,22 @@ struct Params {
   int blk_T, blk_H, blk_B, blk_tiles;
   int blk_col0;  // first column of the fused [Q | K | V] space this GEMM's columns start at
   int blk_qk8;   // Q and K as E4M3 (16 x value): 16-byte groups of 16 columns per row
+  float2* ln_part;  // per (row, column tile): (mean, M2) of the results, or null
 };
 
 // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), with
 // the hardware tanh (one MUFU operation; relative error about 2^-11, the F16
-// output's own rounding).
-__device__ __forceinline__ float gelu_tanh(float x) {
-  const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-  float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(u));
-  const float hx = 0.5f * x;
-  return fmaf(hx, t, hx);
+// output's own rounding). Two values at a time, with the two-lane F32 instructions.
+__device__ __forceinline__ void gelu_tanh_x2(float& x0, float& x1) {
+  float q0, q1, u0, u1, t0, t1, h0, h1;
+  mul_x2(q0, q1, x0, x1, x0, x1);                                  // x^2
+  mul_x2(q0, q1, q0, q1, 0.044715f, 0.044715f);                    // 0.044715 x^2
+  fma_x2(u0, u1, q0, q1, x0, x1, x0, x1);                          // x + 0.044715 x^3
+  mul_x2(u0, u1, u0, u1, 0.7978845608028654f, 0.7978845608028654f);
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(u0));
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(u1));
+  mul_x2(h0, h1, x0, x1, 0.5f, 0.5f);
+  fma_x2(x0, x1, h0, h1, t0, t1, h0, h1);
 }
 
 __device__ __forceinline__ void load8h(const __half* p, float* f) {
@@ -123,8 +132,7 @@ __device__ __forceinline__ void add8h(const uint4& v, float* f) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 t = __half22float2(h[i]);
-    f[2 * i] += t.x;
-    f[2 * i + 1] += t.y;
+    add_x2(f[2 * i], f[2 * i + 1], f[2 * i], f[2 * i + 1], t.x, t.y);
   }
 }
 
@@ -176,9 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* epi = smem + C::kStages * C::kStage;  // [4 warps][2] out blocks, then [4 warps][2] residual blocks
+  uint8_t* epi = smem + C::kStages * C::kStage;  // [epilogue warp][ring] 32 x 32 blocks
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::kEpiBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5 + 4 * C::kEpiRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5 + kEpiWarps * C::kEpiRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_tfull = bar_empty + 8 * C::kStages;
   const uint32_t bar_tempty = bar_tfull + 16;
   const uint32_t bar_drain = bar_tempty + 16;
-  const uint32_t bar_res = bar_drain + 8;  // [4 warps][ring]
+  const uint32_t bar_res = bar_drain + 8;  // [epilogue warp][ring]
 
   // Work items: tiles, or (PAIR) 256-row tiles shared by the two CTAs of a cluster.
   const int aug_blocks = (!FP8 && p.ln_aug) ? 1 : 0;  // folded LayerNorm's extra K block
@@ -204,10 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
-      mbar_init(bar_tempty + 8 * a, PAIR ? 256 : 128);  // every epilogue thread (of both CTAs) arrives
+      mbar_init(bar_tempty + 8 * a, (PAIR ? 64 : 32) * kEpiWarps);  // every epilogue thread (of both CTAs) arrives
     }
     mbar_init(bar_drain, 1);
-    for (int i = 0; i < 4 * C::kEpiRing; ++i) mbar_init(bar_res + 8 * i, 1);
+    for (int i = 0; i < kEpiWarps * C::kEpiRing; ++i) mbar_init(bar_res + 8 * i, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -386,43 +394,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // Epilogue: warp ew owns TMEM lanes 32*sub .. +31, i.e. rows row0 .. row0+31 of
-    // each tile; each 32-column chunk is staged as a 32 x 32 block in shared memory
-    // (64-byte rows with the 64-byte swizzle for F16, 32-byte rows with the 32-byte
-    // swizzle for E4M3) and written by one TMA store, which also clips the M / N tails.
-    const int sub = warp & 3, ew = warp - 2;
-    // Ring of kEpiRing blocks per warp; chunk q (counted over all of this warp's tiles)
+    // each tile, and of them the 32-column chunks c = half, half + 2, ...; each chunk is
+    // staged as a 32 x 32 block in shared memory (64-byte rows with the 64-byte swizzle
+    // for F16, 32-byte rows with the 32-byte swizzle for E4M3) and written by one TMA
+    // store, which also clips the M / N tails.
+    const int sub = warp & 3, ew = warp - 2, half = ew >> 2;
+    // Ring of kEpiRing blocks per warp; chunk q (counted over all of this warp's chunks)
     // uses block q % kEpiRing. With a residual, the residual block of chunk q is
-    // loaded there two chunks ahead, the result overwrites it in place and the TMA
-    // store of the result reads it; the load of chunk q + 2 reuses the block of chunk
-    // q - 2 once that chunk's store has read it.
+    // loaded there kResAhead chunks ahead, the result overwrites it in place and the
+    // TMA store of the result reads it; the load of chunk q + kResAhead reuses the
+    // block of chunk q + kResAhead - kEpiRing once that chunk's store has read it.
+    constexpr int kResAhead = C::kEpiRing - 1;
     uint8_t* ring = epi + ew * C::kEpiRing * C::kEpiBlock;
     const uint32_t rbar = bar_res + 8 * C::kEpiRing * ew;
     // residual loads in flight per block, with the phase parity that completes them
     uint32_t res_issued = 0, res_par = 0;
     // prefetch cursor: next chunk whose residual is to be loaded (work item, chunk, counter)
-    int pit = it0, pc = 0, pq = 0;
+    int pit = it0, pc = half, pq = 0;
     auto prefetch_upto = [&](int qmax) {  // issue residual loads for chunks pq .. qmax
       while (p.has_res && pq <= qmax && pit < num_items) {
         int mt2, nt2;
         tile_of<PAIR>(p, pit, rank, mt2, nt2);
+        if (pc >= tile_chunks(p, nt2, BN)) {  // no (more) chunks of this warp in the tile
+          pc = half;
+          pit += it_step;
+          continue;
+        }
         const int kb = pq % C::kEpiRing;
         res_issued |= 1u << kb;
         res_par = (res_par & ~(1u << kb)) | ((uint32_t(pq / C::kEpiRing) & 1u) << kb);
         if (lane == 0) {
-          bulk_wait_read<C::kEpiRing - 3>();  // the store that last read this block is done
+          bulk_wait_read<C::kEpiRing - 1 - kResAhead>();  // the store that last read this block is done
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(rbar + 8 * kb, C::kEpiBlock);
           tma_load_2d(smem_u32(ring + kb * C::kEpiBlock), &tmR, rbar + 8 * kb, nt2 * BN + 32 * pc,
                       mt2 * kBM + sub * 32);
         }
         ++pq;
-        if (++pc >= tile_chunks(p, nt2, BN)) {
-          pc = 0;
-          pit += it_step;
-        }
+        pc += 2;
       }
     };
-    prefetch_upto(1);
+    prefetch_upto(kResAhead - 1);
     int q = 0;  // chunk counter of this warp: selects blocks and parities
     int local = 0;
     bool ok = true;
@@ -447,13 +459,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulators are in registers, so their latency hides behind chunk c's math.
       uint32_t r[32];
       uint4 bq[4];
-      tmem_ld32(tbase, r);
-      load_bias(p, n0, bq);
+      if (half < nch) {
+        tmem_ld32(tbase + 32 * half, r);
+        load_bias(p, n0 + 32 * half, bq);
+      }
+      // row statistics of this tile for the next LayerNorm: sums of x - x0 and of its
+      // square, x0 = the row's first value in the tile (a shift that keeps the sums small)
+      float st_x0 = 0.0f, st_s1 = 0.0f, st_s2 = 0.0f, st_s1b = 0.0f, st_s2b = 0.0f;
 #pragma unroll 1
-      for (int c = 0; c < nch; ++c, ++q) {
+      for (int c = half; c < nch; c += 2, ++q) {
         const int kb = q % C::kEpiRing;
         uint8_t* blk = ring + kb * C::kEpiBlock;
-        prefetch_upto(q + 2);
+        prefetch_upto(q + kResAhead);
         const int n = n0 + 32 * c;
         const int ngroups = min(4, (p.N - n) / 8);  // groups of 8 columns below N
         tmem_ld_wait(r);
@@ -464,13 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 t = __half22float2(h[i]);
-            v[8 * g + 2 * i] = fmaf(__uint_as_float(r[8 * g + 2 * i]), row_scale, t.x);
-            v[8 * g + 2 * i + 1] = fmaf(__uint_as_float(r[8 * g + 2 * i + 1]), row_scale, t.y);
+            fma_x2(v[8 * g + 2 * i], v[8 * g + 2 * i + 1], __uint_as_float(r[8 * g + 2 * i]),
+                   __uint_as_float(r[8 * g + 2 * i + 1]), row_scale, row_scale, t.x, t.y);
           }
         }
-        if (c + 1 < nch) {
-          tmem_ld32(tbase + 32 * (c + 1), r);
-          load_bias(p, n + 32, bq);
+        if (c + 2 < nch) {
+          tmem_ld32(tbase + 32 * (c + 2), r);
+          load_bias(p, n + 64, bq);
         }
         if (p.pos) {
           const size_t poff = size_t(row % p.pos_rows) * size_t(p.N) + size_t(n);
@@ -485,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (p.act == SV_ACT_GELU_TANH) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+          for (int i = 0; i < 16; ++i) gelu_tanh_x2(v[2 * i], v[2 * i + 1]);
         }
         if (p.has_res) {
           if (!__all_sync(0xffffffffu, mbar_wait<kSleepEpi>(rbar + 8 * kb, uint32_t(q / C::kEpiRing) & 1u, abort_flag, p.err))) {
@@ -499,6 +516,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             add8h(u, v + 8 * g);
           }
           __syncwarp();  // every lane has read its residual row before the block is overwritten
+        }
+        if (p.ln_part) {  // two-lane sums: (even, odd) columns
+          if (c == half) st_x0 = v[0];
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if (g < ngroups) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                float d0, d1;
+                add_x2(d0, d1, v[8 * g + 2 * i], v[8 * g + 2 * i + 1], -st_x0, -st_x0);
+                add_x2(st_s1, st_s1b, st_s1, st_s1b, d0, d1);
+                fma_x2(st_s2, st_s2b, d0, d1, d0, d1, st_s2, st_s2b);
+              }
+            }
         }
         if (p.blk) {  // head-blocked layout for attention: 16-byte stores, consecutive rows contiguous
           if (row < p.M) {
@@ -573,6 +604,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_store_2d(&tmC, smem_u32(blk), n, row0);
           bulk_commit();
         }
+      }
+      if (p.ln_part && ok && row < p.M && half < nch) {  // (mean, M2) of this row's columns of the tile
+        const int w = min(BN, p.N - n0);
+        int cols = 0;  // this warp's columns of the tile
+        for (int c = half; c < nch; c += 2) cols += min(32, w - 32 * c);
+        const float s1 = st_s1 + st_s1b, m1 = s1 / float(cols);
+        p.ln_part[(size_t(row) * p.n_tiles + nt) * 2 + half] =
+            make_float2(st_x0 + m1, fmaxf(st_s2 + st_s2b - s1 * m1, 0.0f));
       }
       tc_fence_before();
       if (PAIR)
@@ -832,6 +871,11 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.blk_B = e.blk_B;
   p.blk_col0 = e.blk_col0;
   p.blk_qk8 = e.blk_qk8;
+  p.ln_part = e.ln_part;
+  if (e.ln_part && (e.blk_out || 2 * p.n_tiles > kMaxLnTiles)) {
+    set_error("gemm: row statistics need a row-major output of at most %d column tiles", kMaxLnTiles / 2);
+    return SV_ERR_INVALID_ARG;
+  }
   p.blk_tiles = (e.blk_T + 127) / 128;
   p.act = e.act;
   p.out_e4m3 = e.out_e4m3;

@@ -50,11 +50,21 @@ struct GemmEpi {
   // LayerNorm of A folded in (A is the LayerNorm input, W already scaled by gamma):
   // the GEMM runs one more K block of 16, ln_aug_a [M, 16] . ln_aug_w [N, 16]^T =
   // -mean_m s_n, and the epilogue scales row m by ln_r[m] before adding `bias` (b').
-  // Single-CTA tiles and F16 operands only.
+  // F16 operands only.
   const float* ln_r = nullptr;         // [M]
   const __half* ln_aug_a = nullptr;    // [M, 16]
   const __half* ln_aug_w = nullptr;    // [N, 16]
+  // Row statistics of the output for the next LayerNorm: for each row m, column tile
+  // t (bn columns, the last one N - t bn) and half h (the tile's 32-column chunks
+  // c = h, h + 2, ...; absent when the tile has no such chunk),
+  // ln_part[(m * n_tiles + t) * 2 + h] = (mean, sum of squared deviations from that
+  // mean) of those F32 results (after bias, positions and residual).
+  // ln_finalize_launch merges them.
+  float2* ln_part = nullptr;
 };
+// Statistics entries per row that GemmEpi::ln_part can hold (two per column tile:
+// 1152 columns in tiles of >= 64).
+constexpr int kMaxLnTiles = 64;
 
 // The operand side of a GEMM: tensor maps for A and W plus the sizes.
 struct GemmOperands {
@@ -107,6 +117,11 @@ sv_status layernorm_launch(const __half* x, const __half* g, const __half* b, vo
 // Row statistics only, for a LayerNorm folded into a GEMM: r[m] = 1/sqrt(var + eps)
 // and aug[m, 0..15] = (-mean_hi, -mean_hi, -mean_lo, 0, ...) in F16.
 sv_status ln_stats_launch(const __half* x, float* r, __half* aug, int rows, int width, float eps, cudaStream_t s);
+// The same r and aug from a GEMM epilogue's per-tile row statistics (GemmEpi::ln_part):
+// part[rows, tiles, 2] of (mean, M2) over the two chunk sets of tiles of tile_w columns
+// (the last width - (tiles-1) tile_w).
+sv_status ln_finalize_launch(const float2* part, int tiles, int tile_w, float* r, __half* aug, int rows, int width,
+                             float eps, cudaStream_t s);
 // W <- W * gamma (per column k, in place, F16); w_aug[n, 0..15] = (s_hi, s_lo, s_hi, 0, ...)
 // with s = sum_k W'[n, k]; b_out[n] = b[n] (0 if null) + sum_k beta[k] W[n, k] (original W), F16.
 sv_status fold_ln_launch(__half* W, const __half* gamma, const __half* beta, const __half* b, __half* w_aug,
