@@ -302,24 +302,25 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, int* err) {
 // Chan, Golub and LeVeque (1979): n = na + nb, d = mean_b - mean_a,
 // mean = mean_a + d nb / n, M2 = M2a + M2b + d^2 na nb / n; then var = M2 / width
 // (biased, as the LayerNorm kernel) and the same r / aug outputs as its statistics mode.
-__global__ void __launch_bounds__(256) ln_finalize_kernel(const float2* __restrict__ part, int tiles, int tile_w,
+__global__ void __launch_bounds__(128) ln_finalize_kernel(const float2* __restrict__ part, int tiles, int tile_w,
                                                          float* __restrict__ r, __half* __restrict__ aug,
                                                          int rows, int width, float eps) {
-  const int row = int(blockIdx.x) * 256 + int(threadIdx.x);
+  const int row = int(blockIdx.x) * 128 + int(threadIdx.x);
   if (row >= rows) return;
   const float2* pr = part + size_t(row) * size_t(2 * tiles);
   float n = 0.0f, mean = 0.0f, m2 = 0.0f;
   for (int t = 0; t < tiles; ++t) {
-    const int w = min(tile_w, width - t * tile_w), chunks = (w + 31) / 32;
+    const int w = min(tile_w, width - t * tile_w), chunks = (w + 31) / 32, last = w - 32 * (chunks - 1);
+#pragma unroll
     for (int h = 0; h < 2; ++h) {
-      int cols = 0;
-      for (int c = h; c < chunks; c += 2) cols += min(32, w - 32 * c);
-      if (cols == 0) continue;
+      // columns of chunks h, h + 2, ... (the last chunk may be partial)
+      const int cols = 32 * ((chunks - h + 1) / 2) - (((chunks - 1) & 1) == h ? 32 - last : 0);
+      if (cols <= 0) continue;
       const float nb = float(cols);
       const float2 q = __ldg(pr + 2 * t + h);
-      const float nn = n + nb, d = q.x - mean;
-      mean = fmaf(d, nb / nn, mean);
-      m2 += q.y + d * d * (n * nb / nn);
+      const float nn = n + nb, d = q.x - mean, f = __fdividef(nb, nn);
+      mean = fmaf(d, f, mean);
+      m2 += q.y + d * d * (n * f);
       n = nn;
     }
   }
@@ -416,7 +417,7 @@ sv_status ln_stats_launch(const __half* x, float* stats_r, __half* stats_aug, in
 
 sv_status ln_finalize_launch(const float2* part, int tiles, int tile_w, float* r, __half* aug, int rows, int width,
                              float eps, cudaStream_t s) {
-  ln_finalize_kernel<<<unsigned((rows + 255) / 256), 256, 0, s>>>(part, tiles, tile_w, r, aug, rows, width, eps);
+  ln_finalize_kernel<<<unsigned((rows + 127) / 128), 128, 0, s>>>(part, tiles, tile_w, r, aug, rows, width, eps);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "ln_finalize launch");
 }
