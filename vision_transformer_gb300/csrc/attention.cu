@@ -256,6 +256,8 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();  // Q, K, V are written by the previous kernel
 
   if (warp == 0) {
     if (lane == 0) {
@@ -633,8 +635,7 @@ sv_status attention_launch_cfg(const CUtensorMap& tmo, const Params& p, int grid
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
     attr_set = true;
   }
-  kern<<<unsigned(grid), kThreads, L::kBytes, s>>>(tmo, p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(kern, dim3(unsigned(grid)), dim3(kThreads), L::kBytes, s, tmo, p);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return SV_OK;
 }

@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(256, CPL <= 9 ? 4 : 1) layernorm_kernel(const 
                                                         const __half* __restrict__ bta, void* __restrict__ y,
                                                         int rows, int width, float eps, int out_e4m3,
                                                         float* __restrict__ stats_r, __half* __restrict__ stats_aug) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;  // half-warp (row of the block), its lane
   const long row0 = long(blockIdx.x) * 16 + hw;
   const bool live = row0 < rows;
@@ -144,6 +146,8 @@ __global__ void __launch_bounds__(256, CPL <= 9 ? 4 : 1) layernorm_kernel(const 
 // moves two values (p*C is even for the 3-channel images of the path).
 __global__ void pack_patches_kernel(const __half2* __restrict__ img, __half2* __restrict__ pix, long pairs, int side,
                                     int C, int p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= pairs) return;
   const int G = side / p, P = p * p * C, run = p * C;
@@ -161,6 +165,8 @@ __global__ void pack_patches_kernel(const __half2* __restrict__ img, __half2* __
 // columns P..Kp-1 (the K tail both GEMM operands share). One thread per 4 values.
 __global__ void pad_pixels_kernel(const __half* __restrict__ pix, void* __restrict__ out, long rows, int P, int Kp,
                                   int out_e4m3) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
   const int cpr = Kp >> 2;
   if (i >= rows * cpr) return;
@@ -207,6 +213,8 @@ constexpr int kMapKeyGroups = 14;
 __global__ void __launch_bounds__(kMapThreads) map_attn_kernel(const __half* __restrict__ q,
                                                                const __half* __restrict__ kv, void* __restrict__ out,
                                                                int T, int D, float scale_log2, int out_e4m3) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ float sm[];
   float* s = sm;        // [T]
   float* red = sm + T;  // [kMapKeyGroups][72]
@@ -305,6 +313,8 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, int* err) {
 __global__ void __launch_bounds__(128) ln_finalize_kernel(const float2* __restrict__ part, int tiles, int tile_w,
                                                          float* __restrict__ r, __half* __restrict__ aug,
                                                          int rows, int width, float eps) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int row = int(blockIdx.x) * 128 + int(threadIdx.x);
   if (row >= rows) return;
   const float2* pr = part + size_t(row) * size_t(2 * tiles);
@@ -381,7 +391,9 @@ __global__ void __launch_bounds__(256) fold_ln_kernel(__half* __restrict__ W, co
 template <int CPL>
 void ln_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width, float eps,
                int out_e4m3, float* stats_r, __half* stats_aug, cudaStream_t s) {
-  layernorm_kernel<CPL><<<(rows + 15) / 16, 256, 0, s>>>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug);
+  // a launch error stays pending for the caller's cudaGetLastError
+  launch_pdl(layernorm_kernel<CPL>, dim3(unsigned((rows + 15) / 16)), dim3(256), 0, s, x, g, b, y, rows, width, eps,
+             out_e4m3, stats_r, stats_aug);
 }
 
 }  // namespace
@@ -417,8 +429,8 @@ sv_status ln_stats_launch(const __half* x, float* stats_r, __half* stats_aug, in
 
 sv_status ln_finalize_launch(const float2* part, int tiles, int tile_w, float* r, __half* aug, int rows, int width,
                              float eps, cudaStream_t s) {
-  ln_finalize_kernel<<<unsigned((rows + 127) / 128), 128, 0, s>>>(part, tiles, tile_w, r, aug, rows, width, eps);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(ln_finalize_kernel, dim3(unsigned((rows + 127) / 128)), dim3(128), 0, s, part, tiles, tile_w,
+                             r, aug, rows, width, eps);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "ln_finalize launch");
 }
 
@@ -431,16 +443,15 @@ sv_status fold_ln_launch(__half* W, const __half* g, const __half* be, const __h
 
 sv_status pack_patches_launch(const __half* img, __half* pix, int B, int side, int C, int p, cudaStream_t s) {
   const long pairs = long(B) * side * side * C / 2;
-  pack_patches_kernel<<<unsigned((pairs + 255) / 256), 256, 0, s>>>(reinterpret_cast<const __half2*>(img),
-                                                                   reinterpret_cast<__half2*>(pix), pairs, side, C, p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(pack_patches_kernel, dim3(unsigned((pairs + 255) / 256)), dim3(256), 0, s,
+                             reinterpret_cast<const __half2*>(img), reinterpret_cast<__half2*>(pix), pairs, side, C, p);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "pack_patches launch");
 }
 
 sv_status pad_pixels_launch(const __half* pix, void* out, long rows, int P, int Kp, int out_e4m3, cudaStream_t s) {
   const long n = rows * (Kp / 4);
-  pad_pixels_kernel<<<unsigned((n + 255) / 256), 256, 0, s>>>(pix, out, rows, P, Kp, out_e4m3);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(pad_pixels_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, s, pix, out, rows, P, Kp,
+                             out_e4m3);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "pad_pixels launch");
 }
 
@@ -467,9 +478,8 @@ sv_status map_attn_launch(const __half* q, const __half* kv, void* out, int B, i
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(map_attn)");
     attr = smem;
   }
-  map_attn_kernel<<<dim3(H, B), kMapThreads, smem, s>>>(q, kv, out, T, H * 72, scale * 1.4426950408889634f,
-                                                         out_e4m3);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(map_attn_kernel, dim3(unsigned(H), unsigned(B)), dim3(kMapThreads), smem, s, q, kv, out, T,
+                             H * 72, scale * 1.4426950408889634f, out_e4m3);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "map_attn launch");
 }
 

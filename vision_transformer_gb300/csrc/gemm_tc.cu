@@ -239,6 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();  // operands, residual and statistics come from earlier kernels
 
   if (warp == 0) {
     if (lane == 0) {
@@ -652,18 +654,24 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
   const int slots = PAIR ? num_sms() / 2 : num_sms();  // one CTA (PAIR: one two-CTA cluster) per SM (pair)
   const int units = items < slots ? items : slots;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(unsigned(PAIR ? 2 * units : units), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
+  // programmatic stream serialization: the prologue (barriers, TMEM, tensor-map
+  // prefetch) may overlap the previous kernel's tail; the kernel waits before any
+  // global access
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (PAIR) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   const CUtensorMap& tr = g.has_res ? g.tr : g.tc;
   const CUtensorMap& twt = (PAIR && g.tail_n) ? g.tw_tail : g.tw;

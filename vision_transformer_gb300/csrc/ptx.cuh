@@ -145,6 +145,15 @@ __device__ __forceinline__ void mul_x2(float& d0, float& d1, float a0, float a1,
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// Programmatic dependent launch. A kernel launched with the programmatic stream
+// serialization attribute may start while the previous kernel in its stream is
+// still running: it calls pdl_wait() before its first global-memory access (the
+// wait returns once that kernel has completed and its writes are visible), and
+// pdl_launch_dependents() lets the next kernel start its own prologue. Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Proxy fence: generic-proxy writes to shared memory become visible to the
 // async proxy (TMA, tensor core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

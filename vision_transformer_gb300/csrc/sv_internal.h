@@ -96,6 +96,23 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
 sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e);
 sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s);
 
+// Launches kern with programmatic stream serialization (the kernel must call
+// pdl_wait() before touching global memory; see ptx.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---- attention (attention.cu)
 // Head-blocked Q/K/V: block (which, b, h, tile) at index ((which*B + b)*H + h)*tiles + tile
 // (which 0 = Q, 1 = K, 2 = V; tiles of 128 tokens), each block 9 column groups x 128 rows x
