@@ -31,18 +31,21 @@
 //     masked to -inf before the row maximum, so their probability is exactly 0;
 //   - query rows past the last token are computed but never stored.
 //
-// CTA = (256 queries as two 128-row tiles, head, image), 320 threads:
-//   warp 0      bulk copies: Q (both tiles) once, then K and V tiles of 128
-//               keys, each into 2 stages with its own release;
-//   warp 1      TMEM owner + MMA issuer: per softmax group w, S_w(j) = Q_w K_j^T
-//               (M 128, N 128, K 80) and O_w(j) = P_w(j) V_j (M 128, N 80, K 128);
-//   warps 2..5  softmax group 0, warps 6..9 softmax group 1: one thread per
-//               query row reads its S row from TMEM, writes P (F16) to shared
-//               memory and folds O into an F32 register accumulator with the
-//               online-softmax rescale; the softmax denominator comes out of
-//               the P V product (a column of ones in V's pad group). The two
-//               groups ping-pong: while one computes exponentials the tensor
-//               core serves the other.
+// Persistent CTAs (one per SM) walk work items of (256 queries as two 128-row
+// tiles, head, image); 352 threads:
+//   warp 0      bulk copies: Q (both tiles) per item, then K and V tiles of 128
+//               keys into 3 + 3 stages, each with its own release;
+//   warps 1, 2  MMA issuers, one per softmax group w: S_w = Q_w K_j^T
+//               (M 128, N 128) into TMEM, then O_w += P_w V_j (M 128, N 80) in
+//               two 64-key halves, O_w kept in TMEM for the whole item;
+//   warps 3..6  softmax group 0, warps 7..10 softmax group 1: one thread per
+//               query row reads its S row from TMEM once (S is then free for the
+//               next product), writes P (F16) to shared memory, and rescales O
+//               in TMEM only when the row maximum grows by more than 2^15; the
+//               softmax denominator comes out of the P V product (a column of
+//               ones in V's pad group). An item's output rows are staged in shared
+//               memory and written by a TMA store during the next item.
+
 #include <cuda_fp8.h>
 
 #include <cstring>

@@ -17,11 +17,15 @@
 //               (clusters of 2) that share one M = 256 MMA (cta_group::2):
 //               each CTA stages its 128 rows of A and half of the W tile, the
 //               leader issues the MMAs, each CTA's TMEM holds its 128 rows;
-//   warps 2..5  epilogue: tcgen05.ld of 32 columns at a time (the next
-//               chunk's load in flight during this chunk's math), fused math,
-//               the 32 x 32 result block staged in swizzled shared memory and
-//               written by a TMA store; residual blocks arrive by TMA one
-//               chunk ahead.
+//   warps 2..9  epilogue, two warps per TMEM lane quarter taking alternate
+//               32-column chunks: tcgen05.ld of a chunk (the warp's next chunk
+//               in flight during this chunk's math), fused math, the 32 x 32
+//               result block staged in swizzled shared memory and written by a
+//               TMA store; residual blocks arrive by TMA one chunk ahead; the
+//               GEMMs that write the residual stream also leave per-tile row
+//               statistics for the next LayerNorm.
+// Launched with programmatic stream serialization: the prologue overlaps the
+// previous kernel, global memory is touched only after griddepcontrol.wait.
 // F16 operands use kind::f16 (K = 16 per instruction); E4M3 operands use
 // kind::f8f6f4 (K = 32 per instruction) with the dequantisation scale
 // applied to the accumulator. All waits are bounded (ptx.cuh).
