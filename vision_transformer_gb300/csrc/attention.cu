@@ -406,8 +406,11 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
           uint4 wv;
           __half2* hw = reinterpret_cast<__half2*>(&wv);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            hw[i] = __floats2half2_rn(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+          for (int i = 0; i < 4; ++i) {
+            float a, b;
+            mul_x2(a, b, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), inv, inv);
+            hw[i] = __floats2half2_rn(a, b);
+          }
           *reinterpret_cast<uint4*>(stg + 16 * g) = wv;
         } else if (tq < T) {
           uint2 wv;
@@ -529,7 +532,12 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
           asm volatile("" : "+r"(e[0]), "+r"(e[1]), "+r"(e[2]), "+r"(e[3]), "+r"(e[4]), "+r"(e[5]), "+r"(e[6]),
                        "+r"(e[7]));
 #pragma unroll
-          for (int i = 0; i < 8; ++i) e[i] = __float_as_uint(__uint_as_float(e[i]) * f);
+          for (int i = 0; i < 4; ++i) {
+            float a, b;
+            mul_x2(a, b, __uint_as_float(e[2 * i]), __uint_as_float(e[2 * i + 1]), f, f);
+            e[2 * i] = __float_as_uint(a);
+            e[2 * i + 1] = __float_as_uint(b);
+          }
           tmem_st8(o_tm + 8 * c, e);
         }
         tmem_st_wait();
@@ -558,9 +566,10 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
             __half2* hw = reinterpret_cast<__half2*>(&wv);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float p0 = ex2(fmaf(__uint_as_float(sv[2 * half + cc][8 * g + 2 * i]), sl2, -m));
-              const float p1 = ex2(fmaf(__uint_as_float(sv[2 * half + cc][8 * g + 2 * i + 1]), sl2, -m));
-              hw[i] = __floats2half2_rn(p0, p1);
+              float x0, x1;  // scale log2(e) s - m for two keys in one two-lane FMA
+              fma_x2(x0, x1, __uint_as_float(sv[2 * half + cc][8 * g + 2 * i]),
+                     __uint_as_float(sv[2 * half + cc][8 * g + 2 * i + 1]), sl2, sl2, -m, -m);
+              hw[i] = __floats2half2_rn(ex2(x0), ex2(x1));
             }
             *reinterpret_cast<uint4*>(ph + (4 * cc + g) * kGroupBytes + r * 16) = wv;
           }
