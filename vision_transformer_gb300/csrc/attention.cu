@@ -381,11 +381,12 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
     uint8_t* pbuf = smem + kOffP + w * kPBytes;
     const float sl2 = QK8 ? p.scale_log2 * (1.0f / 256.0f) : p.scale_log2;  // E4M3 operands hold 16 q, 16 k
     const int D = p.H * kDh;
-    // An item's output rows: the final O (with its row sum in column 72) of the group's
-    // query tile, read from TMEM, scaled by 1 / row sum. F16 rows are staged as this
-    // warp's 32 x 72 block in the group's P buffer (free once the item's last P V has
-    // finished) and written by one TMA store that clips the rows past the image's last
-    // token; E4M3 rows are stored directly.
+    // An item's output rows, at the end of its last tile (the S row is no longer held,
+    // so all 80 columns of O are read at once): the final O (with its row sum in column
+    // 72) of the group's query tile, read from TMEM once its last P V has finished,
+    // scaled by 1 / row sum. F16 rows are staged as this warp's 32 x 72 block in the
+    // group's P buffer (free once that P V has finished) and written by one TMA store
+    // that clips the rows past the image's last token; E4M3 rows are stored directly.
     auto finish_item = [&](int n, int tl) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), tl & 1, abort_flag, p.err))) return false;
       tc_fence_after();
@@ -394,14 +395,18 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
       const int tq = tq0 + lane;
       uint8_t* stg = pbuf + sub * (32 * kDh * 2) + lane * (kDh * 2);
       uint8_t* dst8 = static_cast<uint8_t*>(p.out) + (size_t(I.b) * size_t(T) + size_t(tq)) * size_t(D) + size_t(I.h) * kDh;
-      // columns 64..79 first: column 72 holds the row sum
-      uint32_t e[16];
-      tmem_ld16(o_tm + 64, e);
+      uint32_t o[5][16];
+#pragma unroll
+      for (int c = 0; c < 5; ++c) tmem_ld16(o_tm + 16 * c, o[c]);
       tmem_ld_wait();
-      asm volatile("" : "+r"(e[0]), "+r"(e[1]), "+r"(e[2]), "+r"(e[3]), "+r"(e[4]), "+r"(e[5]), "+r"(e[6]), "+r"(e[7]),
-                   "+r"(e[8]));
-      const float inv = 1.0f / __uint_as_float(e[8]);
-      auto emit8 = [&](const uint32_t* v, int g) {  // output columns 8 g .. 8 g + 7
+#pragma unroll
+      for (int c = 0; c < 5; ++c)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(o[c][i]));  // no use before the wait
+      const float inv = 1.0f / __uint_as_float(o[4][8]);  // column 72: the row sum
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {  // output columns 8 g .. 8 g + 7
+        const uint32_t* v = &o[g >> 1][8 * (g & 1)];
         if (!p.out_e4m3) {
           uint4 wv;
           __half2* hw = reinterpret_cast<__half2*>(&wv);
@@ -422,18 +427,6 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
                                             __NV_SATFINITE, __NV_E4M3);
           *reinterpret_cast<uint2*>(dst8 + 8 * g) = wv;
         }
-      };
-      emit8(e, 8);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[16];
-        tmem_ld16(o_tm + 16 * c, v);
-        tmem_ld_wait();
-        asm volatile("" : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
-                     "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
-                     "+r"(v[14]), "+r"(v[15]));
-        emit8(v, 2 * c);
-        emit8(v + 8, 2 * c + 1);
       }
       tc_fence_before();
       mbar_arrive(bar(kBarOEmpty + w));  // the next item's first P V may overwrite O
@@ -451,8 +444,7 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
     // in TMEM; the softmax denominator accumulates in O's column 72.
     float m = -INFINITY;
     bool ok = true;
-    int pend = -1;      // item whose output rows are still to be written (its last tile: pend_t)
-    int pend_t = 0;
+    bool pend = false;  // the previous item's output rows were staged at the end of its last tile
     int staged = 0;     // items whose output went through the staging rows
 
     for (int t = 0; t < total && ok; ++t) {
@@ -475,14 +467,11 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
       reg_fence(sv[3]);
       tc_fence_before();
       mbar_arrive(bar(kBarSEmpty + w));
-      // The previous item's output, now that its last P V has had time to finish.
+      // The previous item's staged output: its store must read the staging rows before
+      // this tile's P overwrites them.
       bool wait_stage = false;
-      if (pend >= 0) {
-        if (!finish_item(pend, pend_t)) {
-          ok = false;
-          break;
-        }
-        pend = -1;
+      if (pend) {
+        pend = false;
         if (!p.out_e4m3) {
           wait_stage = true;
           if (lane == 0) bulk_wait_read<0>();  // this warp's store has read its staging rows
@@ -580,12 +569,14 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
       }
       if (!ok) break;
 
-      if (j == nkv - 1) {  // the item's output is written during the next item's first tile
-        pend = n;
-        pend_t = t;
+      if (j == nkv - 1) {  // the item's output rows, once its last P V has finished
+        if (!finish_item(n, t)) {
+          ok = false;
+          break;
+        }
+        pend = true;
       }
     }
-    if (ok && pend >= 0) ok = finish_item(pend, pend_t);
     if (lane == 0) bulk_wait_all();  // output stores have read shared memory before the CTA exits
     tmem_ld_wait();
   }
