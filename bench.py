@@ -47,9 +47,9 @@ def flops_per_image(layers: int = L27) -> float:
 # dram__bytes_write.sum from one ncu capture of the four encoder GEMMs of a layer at
 # batch 32 (QKV, output projection, MLP up, MLP down; their mean), valid only for the
 # kernel sources it was taken on (first 16 hex digits of sha256 of each file).
-GEMM_TRAFFIC = {"bytes_per_launch": 211.4e6,
-                "sources": {"vision_transformer_gb300/csrc/gemm_tc.cu": "81a930dc56669215",
-                            "vision_transformer_gb300/csrc/ptx.cuh": "3a8e9a0c16bec909"}}
+GEMM_TRAFFIC = {"bytes_per_launch": 211.8e6,
+                "sources": {"vision_transformer_gb300/csrc/gemm_tc.cu": "ca42acceb54727b8",
+                            "vision_transformer_gb300/csrc/ptx.cuh": "c14a6ba00ae37935"}}
 
 
 def gemm_traffic():
