@@ -98,7 +98,11 @@ sv_status sv_model_dims(int* tokens, int* patch_dim, int* width, int* heads, int
  * dense-GEMM operand in E4M3 at scale 2^-4 (activations quantised by the
  * kernel that produces them), F32 accumulation; LayerNorm statistics,
  * softmax and attention accumulation stay F32 and the residual stream F16 in
- * both modes ("SigLIP ViT benchmark", precision paragraph).
+ * both modes ("SigLIP ViT benchmark", precision paragraph). With F16 the
+ * encoder's LayerNorms are folded into the QKV and MLP-up projections (gamma in
+ * the weights, beta in the bias, the mean subtracted by the tensor core, 1/std
+ * in the epilogue), their row statistics taken from the epilogues of the GEMMs
+ * that write the residual stream.
  * `pixels` needs only 8-byte alignment. The first call at a given batch size
  * and gemm_dtype allocates and caches a device workspace (freed by
  * sv_shutdown); later calls allocate nothing.

@@ -81,24 +81,25 @@ def test_deterministic_and_no_stale_reads(sv, so400m):
     assert np.isfinite(d8).all() and np.array_equal(d8, e8)
 
 
-@pytest.mark.parametrize("dtype", [0, 1])
-def test_unfused_qkv_matches_fused(sv, so400m, dtype):
+@pytest.mark.parametrize("dtype,qk8", [(0, 0), (1, 0), (0, 1)])
+def test_unfused_qkv_matches_fused(sv, so400m, dtype, qk8):
     """Q, K, V as three GEMMs over the fused weight's row slices ("Fused QKV
     projection": fusion changes no math): the same bits as the fused GEMM (each
-    output element's K loop is the same), and within the one-layer tolerance of
-    the oracle."""
+    output element's K loop is the same), also with E4M3 Q and K written by the
+    three epilogues, and within the one-layer tolerance of the oracle."""
     B = 2
     pix = synth.pixels(4, B)
     x = torch.from_numpy(pix).cuda()
     D = sv.sv_model_dims()["width"]
     fused = torch.empty(B, 1, D, dtype=torch.float16, device="cuda")
     split = torch.empty_like(fused)
-    sv.sv_encode(x, fused, B, 2, dtype)
-    sv.sv_encode_ex(x, split, B, 2, dtype, sv.SV_ENCODE_UNFUSED_QKV)
+    extra = sv.SV_ENCODE_FP8_ATTENTION if qk8 else 0
+    sv.sv_encode_ex(x, fused, B, 2, dtype, extra)
+    sv.sv_encode_ex(x, split, B, 2, dtype, sv.SV_ENCODE_UNFUSED_QKV | extra)
     sv.sv_sync()
     a, b = host(fused).reshape(B, -1), host(split).reshape(B, -1)
     assert np.array_equal(a, b)
-    if dtype == 0:
+    if dtype == 0 and not qk8:
         ref = so400m.encode(pix, layers=2)
         assert cosine_rows(b, ref).min() >= 0.9999
 
