@@ -3,9 +3,10 @@
 One step = one forward pass of the whole path (patch-embedding GEMM, 27
 encoder layers, final LayerNorm, MAP pooling) over one batch of synthetic
 pixels, through the library's C ABI. The default workload is the 27-layer
-encoder + MAP at 378 px, F16 GEMM operands, batch 32 per GPU (the regime the
-tensor-core target is quoted in); weights are drawn by the seeded generator
-and resident in HBM; pixels are uniform in [-1, 1].
+encoder + MAP at 378 px, F16 GEMM operands, batch 128 per GPU (the largest
+batch of the throughput sweep; the tensor-core target is quoted for batch >= 32);
+weights are drawn by the seeded generator and resident in HBM; pixels are
+uniform in [-1, 1].
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--dtype f16|e4m3] [--unfused-qkv]
                   [--fp8-attention]
@@ -45,16 +46,22 @@ def flops_per_image(layers: int = L27) -> float:
 
 # DRAM traffic of the dense-GEMM kernel per launch: dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture of the four encoder GEMMs of a layer at
-# batch 32 (QKV, output projection, MLP up, MLP down; their mean), valid only for the
-# kernel sources it was taken on (first 16 hex digits of sha256 of each file).
-GEMM_TRAFFIC = {"bytes_per_launch": 211.8e6,
+# batch 32, F16 (QKV, output projection, MLP up, MLP down; their mean), valid only for
+# the kernel sources it was taken on (first 16 hex digits of sha256 of each file).
+GEMM_TRAFFIC = {"batch": 32, "bytes_per_launch": 211.8e6,
+                "weight_bytes_per_launch": 7.6e6,  # mean F16 weight bytes of the four
                 "sources": {"vision_transformer_gb300/csrc/gemm_tc.cu": "ca42acceb54727b8",
                             "vision_transformer_gb300/csrc/ptx.cuh": "c14a6ba00ae37935"}}
 
 
-def gemm_traffic():
-    """The recorded per-launch DRAM traffic, or None once the kernel sources differ."""
+def gemm_traffic(batch: int, dtype: str):
+    """Per-launch DRAM traffic of the GEMM kernel for this workload, or None once the kernel
+    sources differ from the profiled ones (or for E4M3 operands, never profiled). Other batch
+    sizes scale the capture by rows: activations and outputs grow with the batch, the weights
+    are read once per launch."""
     import hashlib
+    if dtype != "f16":
+        return None
     for rel, h in GEMM_TRAFFIC["sources"].items():
         try:
             with open(os.path.join(ROOT, rel), "rb") as f:
@@ -62,7 +69,8 @@ def gemm_traffic():
                     return None
         except OSError:
             return None
-    return GEMM_TRAFFIC["bytes_per_launch"]
+    w = GEMM_TRAFFIC["weight_bytes_per_launch"]
+    return w + (GEMM_TRAFFIC["bytes_per_launch"] - w) * batch / GEMM_TRAFFIC["batch"]
 
 
 def measured_peaks() -> dict:
@@ -222,7 +230,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--batch", type=int, default=32, help="images per GPU per step")
+    ap.add_argument("--batch", type=int, default=128, help="images per GPU per step")
     ap.add_argument("--dtype", choices=("f16", "e4m3"), default="f16")
     ap.add_argument("--unfused-qkv", action="store_true", help="Q, K, V as three GEMMs (comparison only)")
     ap.add_argument("--fp8-attention", action="store_true", help="scores on E4M3 Q and K (FP8 attention products)")
@@ -354,8 +362,9 @@ def main():
                                  f"{peaks['source']} dense bf16 burst peak"},
             "roofline": {"kernel": "gemm_tc (all dense-GEMM launches of the step)", "bound": "tensor",
                          "achieved": gemm_tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": gemm_tflops / peak if peak else None, "traffic": gemm_traffic(),
-                         "traffic_unit": "bytes per launch (ncu DRAM read + write, mean of the 4 encoder GEMMs)",
+                         "frac": gemm_tflops / peak if peak else None, "traffic": gemm_traffic(B, args.dtype),
+                         "traffic_unit": "bytes per launch (ncu DRAM read + write, mean of the 4 encoder GEMMs, "
+                                         "captured at batch 32 and scaled by rows to this batch)",
                          "peak_kind": f"{peaks['source']} bf16 sustained"},
             "kernels": kernels,
             "e2e": {"value": e2e_value, "unit": "images/s", "h2d_bytes_per_step": host_img.numel() * 2,
