@@ -494,13 +494,8 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
 #pragma unroll
       for (int k = 0; k < 8; ++k)
 #pragma unroll
-        for (int i = 2; i < 16; i += 2) {
-#ifdef EXP_MAXF
-          mq[k] = fmaxf(mq[k], fmaxf(__uint_as_float(sv[k >> 1][(k & 1) * 16 + i]), __uint_as_float(sv[k >> 1][(k & 1) * 16 + i + 1])));
-#else
+        for (int i = 2; i < 16; i += 2)
           mq[k] = fmax3(mq[k], __uint_as_float(sv[k >> 1][(k & 1) * 16 + i]), __uint_as_float(sv[k >> 1][(k & 1) * 16 + i + 1]));
-#endif
-        }
       const float mx = fmaxf(fmaxf(fmax3(mq[0], mq[1], mq[2]), fmax3(mq[3], mq[4], mq[5])), fmaxf(mq[6], mq[7]));
       const float m_tile = mx * sl2;
       const bool raise = m_tile > m + kSlack;  // always on an item's first tile
