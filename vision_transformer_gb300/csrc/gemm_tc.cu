@@ -40,7 +40,7 @@ namespace sv {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBKBytes = 128;  // K bytes per stage: one 128-byte swizzle row
+constexpr int kSwzBytes = 128;  // one 128-byte swizzle row of K
 // Warp 0 loads, warp 1 issues the MMAs, warps 2 .. 9 run the epilogue: two per
 // TMEM lane quarter, each taking every other 32-column chunk of a tile (with four,
 // the epilogue of a K = 1152 tile took about as long as its main loop).
@@ -60,10 +60,17 @@ constexpr uint32_t kSleepEpi = 1000000;
 // PAIR: the two CTAs of a cluster share one 256-row MMA (cta_group::2): each
 // holds its 128 rows of A and half of the W tile per stage, and the tensor core
 // reads the other half from the peer.
-template <int BN, bool PAIR>
+// ATOMS: 128-byte swizzle rows of K per stage. Two (fewer, larger stages, half the
+// barrier round trips per K) pay for CTA pairs over K = 1152 with L2-resident operands
+// (QKV, MLP up: 4-7% faster); one is better where A streams from DRAM (MLP down) or a
+// single CTA would be left with two stages (output projection).
+template <int BN, bool PAIR, int ATOMS>
 struct Cfg {
-  static constexpr int kStageA = kBM * kBKBytes;
-  static constexpr int kStageB = (PAIR ? BN / 2 : BN) * kBKBytes;
+  static constexpr int kAtomA = kBM * kSwzBytes;                   // one swizzle row of the A tile
+  static constexpr int kAtomB = (PAIR ? BN / 2 : BN) * kSwzBytes;  // of the W tile (this CTA's rows)
+  static constexpr int kStageA = kAtomA * ATOMS;
+  static constexpr int kStageB = kAtomB * ATOMS;
+  static constexpr int kBKBytes = kSwzBytes * ATOMS;  // K bytes per stage
   static constexpr int kStage = kStageA + kStageB;
   // epilogue staging: per epilogue warp a ring of two 32 x 32 blocks (residual in,
   // result out)
@@ -178,14 +185,14 @@ __device__ __forceinline__ void tile_of(const Params& p, int it, int rank, int& 
   mt = PAIR ? 2 * mu + rank : mu;
 }
 
-template <int BN, bool FP8, bool PAIR>
+template <int BN, bool FP8, bool PAIR, int ATOMS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmWt, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmAa,
                    const __grid_constant__ CUtensorMap tmWa, const __grid_constant__ CUtensorMap tmWat,
                    const Params p) {
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIR, ATOMS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + C::kStages * C::kStage;  // [epilogue warp][ring] 32 x 32 blocks
@@ -262,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb = bar_full + 8 * stage;
           const uint32_t sa = smem_u32(smem + stage * C::kStage);
-          const int kc = kb * (FP8 ? 128 : 64);
+          const int kc = kb * (FP8 ? C::kBKBytes : C::kBKBytes / 2);
+          constexpr int kAtomK = FP8 ? kSwzBytes : kSwzBytes / 2;  // K elements of one swizzle row
           if (kb == p.k_blocks) {  // folded LayerNorm: the 16-wide K block (-mean | column sums)
             if (PAIR) {  // each CTA: its 128 rows of the A block, its half of the W block's rows
               const bool narrow = nt == p.n_full && p.tail_n;
@@ -279,18 +287,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (PAIR) {  // both CTAs' copies complete on the leader's barrier
             const uint32_t fb_lead = mapa_shared(fb, 0);
             if (nt == p.n_full && p.tail_n) {  // narrow tile: each CTA holds tail_n / 2 W rows
-              if (leader) mbar_arrive_expect_tx(fb, 2 * (C::kStageA + (p.tail_n / 2) * kBKBytes));
-              tma_load_2d_pair(sa, &tmA, fb_lead, kc, mt * kBM);
-              tma_load_2d_pair(sa + C::kStageA, &tmWt, fb_lead, kc, nt * BN + rank * (p.tail_n / 2));
+              if (leader) mbar_arrive_expect_tx(fb, 2 * (C::kStageA + (p.tail_n / 2) * C::kBKBytes));
+#pragma unroll
+              for (int a = 0; a < ATOMS; ++a) {
+                tma_load_2d_pair(sa + a * C::kAtomA, &tmA, fb_lead, kc + a * kAtomK, mt * kBM);
+                tma_load_2d_pair(sa + C::kStageA + a * C::kAtomB, &tmWt, fb_lead, kc + a * kAtomK,
+                                 nt * BN + rank * (p.tail_n / 2));
+              }
             } else {
               if (leader) mbar_arrive_expect_tx(fb, 2 * C::kStage);
-              tma_load_2d_pair(sa, &tmA, fb_lead, kc, mt * kBM);
-              tma_load_2d_pair(sa + C::kStageA, &tmW, fb_lead, kc, nt * BN + rank * (BN / 2));
+#pragma unroll
+              for (int a = 0; a < ATOMS; ++a) {
+                tma_load_2d_pair(sa + a * C::kAtomA, &tmA, fb_lead, kc + a * kAtomK, mt * kBM);
+                tma_load_2d_pair(sa + C::kStageA + a * C::kAtomB, &tmW, fb_lead, kc + a * kAtomK,
+                                 nt * BN + rank * (BN / 2));
+              }
             }
           } else {
             mbar_arrive_expect_tx(fb, C::kStage);
-            tma_load_2d(sa, &tmA, fb, kc, mt * kBM);
-            tma_load_2d(sa + C::kStageA, &tmW, fb, kc, nt * BN);
+#pragma unroll
+            for (int a = 0; a < ATOMS; ++a) {
+              tma_load_2d(sa + a * C::kAtomA, &tmA, fb, kc + a * kAtomK, mt * kBM);
+              tma_load_2d(sa + C::kStageA + a * C::kAtomB, &tmW, fb, kc + a * kAtomK, nt * BN);
+            }
           }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -350,9 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_f16(d, make_sdesc(sa, 16, 256, 6), make_sdesc(sb, 16, 256, 6), idesc, 1u);
           } else
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {  // 4 instructions x 32 bytes of K
-            const uint64_t ad = make_sdesc(sa + 32 * j, 16, 1024, 2);
-            const uint64_t bd = make_sdesc(sb + 32 * j, 16, 1024, 2);
+          for (int j = 0; j < 4 * ATOMS; ++j) {  // 4 instructions x 32 bytes of K per swizzle row
+            const uint64_t ad = make_sdesc(sa + (j >> 2) * C::kAtomA + 32 * (j & 3), 16, 1024, 2);
+            const uint64_t bd = make_sdesc(sb + (j >> 2) * C::kAtomB + 32 * (j & 3), 16, 1024, 2);
             const uint32_t accum = (kb | j) != 0;
             if (PAIR) {
               if (FP8)
@@ -644,11 +663,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, bool FP8, bool PAIR>
+template <int BN, bool FP8, bool PAIR, int ATOMS = 1>
 sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIR, ATOMS>;
   static bool attr_set = false;
-  auto kern = gemm_tc_kernel<BN, FP8, PAIR>;
+  auto kern = gemm_tc_kernel<BN, FP8, PAIR, ATOMS>;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm)");
@@ -735,7 +754,7 @@ sv_status make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void
 sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int fp8, int box_rows) {
   const uint64_t dims[2] = {uint64_t(K), uint64_t(rows)};
   const uint64_t strides[1] = {uint64_t(K) * (fp8 ? 1u : 2u)};
-  const uint32_t box[2] = {uint32_t(fp8 ? 128 : 64), uint32_t(box_rows)};
+  const uint32_t box[2] = {uint32_t(fp8 ? kSwzBytes : kSwzBytes / 2), uint32_t(box_rows)};
   return make_tmap(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, dims, strides,
                    box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -779,6 +798,8 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
   g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && (K >= 2048 || N >= 2048);
   g->bn = gemm_pick_bn(M, N, K, g->mc);
   if (g->mc && g->bn > kPairMaxBn) g->bn = kPairMaxBn;
+  // two swizzle rows of K per stage for 256-wide CTA-pair tiles over a short K (see Cfg)
+  g->atoms = (g->mc && g->bn == 256 && K <= 2048) ? 2 : 1;
   // A narrower last column tile (N % bn columns) runs MMAs of its own width, rounded
   // up to 16 columns (32 for a CTA pair, whose CTAs hold half of the W rows each).
   const int rem = N % g->bn;
@@ -870,7 +891,7 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.tail_n = g.tail_n;
   p.n_full = g.tail_n ? p.n_tiles - 1 : p.n_tiles;
   p.tail_last = g.tail_last;
-  const int bk = g.fp8 ? 128 : 64;
+  const int bk = (g.fp8 ? kSwzBytes : kSwzBytes / 2) * g.atoms;
   p.k_blocks = (g.K + bk - 1) / bk;
   p.bias = e.bias;
   p.pos = e.pos;
@@ -899,12 +920,14 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
     return SV_ERR_INVALID_ARG;
   }
   p.err = dev_err();
-  const int key = g.bn | (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0);
+  const int key = g.bn | (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0) | (g.atoms == 2 ? 4 : 0);
   switch (key) {
     case 256: return launch_bn<256, false, false>(g, p, s);
     case 257: return launch_bn<256, true, false>(g, p, s);
     case 258: return launch_bn<256, false, true>(g, p, s);
     case 259: return launch_bn<256, true, true>(g, p, s);
+    case 262: return launch_bn<256, false, true, 2>(g, p, s);
+    case 263: return launch_bn<256, true, true, 2>(g, p, s);
     case 192: return launch_bn<192, false, false>(g, p, s);
     case 193: return launch_bn<192, true, false>(g, p, s);
     case 194: return launch_bn<192, false, true>(g, p, s);

@@ -79,6 +79,7 @@ struct GemmOperands {
   int fp8 = 0;
   int bn = 0;
   int mc = 0;  // CTA pairs (clusters of 2) sharing one 256-row MMA
+  int atoms = 1;  // 128-byte swizzle rows of K per pipeline stage (1 or 2)
   int has_res = 0;
   const void* out = nullptr;  // epilogue buffers the output / residual maps describe
   const void* res = nullptr;
