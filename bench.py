@@ -48,9 +48,9 @@ def flops_per_image(layers: int = L27) -> float:
 # dram__bytes_write.sum from one ncu capture of the four encoder GEMMs of a layer at
 # batch 32, F16 (QKV, output projection, MLP up, MLP down; their mean), valid only for
 # the kernel sources it was taken on (first 16 hex digits of sha256 of each file).
-GEMM_TRAFFIC = {"batch": 32, "bytes_per_launch": 211.8e6,
+GEMM_TRAFFIC = {"batch": 32, "bytes_per_launch": 211.2e6,
                 "weight_bytes_per_launch": 7.6e6,  # mean F16 weight bytes of the four
-                "sources": {"vision_transformer_gb300/csrc/gemm_tc.cu": "ca42acceb54727b8",
+                "sources": {"vision_transformer_gb300/csrc/gemm_tc.cu": "c7e1e11134e578b1",
                             "vision_transformer_gb300/csrc/ptx.cuh": "c14a6ba00ae37935"}}
 
 
