@@ -798,8 +798,9 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
   g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && (K >= 2048 || N >= 2048);
   g->bn = gemm_pick_bn(M, N, K, g->mc);
   if (g->mc && g->bn > kPairMaxBn) g->bn = kPairMaxBn;
-  // two swizzle rows of K per stage for 256-wide CTA-pair tiles over a short K (see Cfg)
-  g->atoms = (g->mc && g->bn == 256 && K <= 2048) ? 2 : 1;
+  // two swizzle rows of K per stage for 256-wide CTA-pair tiles over a short K that they
+  // divide (see Cfg; E4M3 over K = 1152 would leave half of its last stage empty)
+  g->atoms = (g->mc && g->bn == 256 && K <= 2048 && K % (2 * (fp8 ? kSwzBytes : kSwzBytes / 2)) == 0) ? 2 : 1;
   // A narrower last column tile (N % bn columns) runs MMAs of its own width, rounded
   // up to 16 columns (32 for a CTA pair, whose CTAs hold half of the W rows each).
   const int rem = N % g->bn;
