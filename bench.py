@@ -286,16 +286,17 @@ def main():
         dist.barrier()
     torch.cuda.synchronize(dev)
     vt.sv_launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]  # one after each step
     with ClockSampler(local) as clk:
-        e0.record(stream)
-        for _ in range(args.steps):
+        ev[0].record(stream)
+        for i in range(args.steps):
             step()
-        e1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize(dev)
     vt.sv_sync(stream)
     launches = vt.sv_launch_count()
-    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    elapsed_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world)
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]  # this rank's batch latencies
     ms_per_step = elapsed_ms / args.steps
     value = B * world / (ms_per_step / 1e3)
 
@@ -366,6 +367,9 @@ def main():
                          "traffic_unit": "bytes per launch (ncu DRAM read + write, mean of the 4 encoder GEMMs, "
                                          "captured at batch 32 and scaled by rows to this batch)",
                          "peak_kind": f"{peaks['source']} bf16 sustained"},
+            "latency_ms": {"mean": ms_per_step, "median": statistics.median(step_ms), "min": min(step_ms),
+                           "max": max(step_ms), "basis": "per-step CUDA events on rank 0's launching "
+                                                         "stream; mean = the timed region's max over ranks / steps"},
             "kernels": kernels,
             "e2e": {"value": e2e_value, "unit": "images/s", "h2d_bytes_per_step": host_img.numel() * 2,
                     "d2h_bytes_per_step": host_out.numel() * 2,
