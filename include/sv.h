@@ -106,6 +106,14 @@ sv_status sv_model_dims(int* tokens, int* patch_dim, int* width, int* heads, int
  * `pixels` needs only 8-byte alignment. The first call at a given batch size
  * and gemm_dtype allocates and caches a device workspace (freed by
  * sv_shutdown); later calls allocate nothing.
+ * Launches: the first call with given (pixels, out, batch, layers, gemm_dtype,
+ * flags) launches its kernels one by one; the second captures the same launch
+ * sequence into a CUDA graph (on an internal stream) and later calls with the
+ * same arguments launch that graph on `stream`: one host call per step, with
+ * identical results. The graphs name the caller's buffers by address, so a
+ * buffer freed and reallocated at the same address must keep its role; the
+ * graphs are dropped by sv_init_weights and sv_shutdown. Calls made while
+ * profiling is on (sv_profile_enable) always launch one by one.
  * Errors: SV_ERR_NOT_INITIALIZED, SV_ERR_INVALID_ARG, SV_ERR_OOM, SV_ERR_CUDA.
  */
 sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int gemm_dtype, void* stream);
@@ -125,12 +133,15 @@ typedef enum {
    * Softmax, the P V product (F16) and the output precision are unchanged; the
    * MAP head's single-query attention is not affected. Combines with either
    * gemm_dtype. */
-  SV_ENCODE_FP8_ATTENTION = 2
+  SV_ENCODE_FP8_ATTENTION = 2,
+  /* Launch the kernels one by one on every call (no step graph; see sv_encode).
+   * The results are the same. */
+  SV_ENCODE_EAGER = 4
 } sv_encode_flags;
 
 /*
  * sv_encode with options: flags is 0 (exactly sv_encode) or any OR of
- * SV_ENCODE_UNFUSED_QKV and SV_ENCODE_FP8_ATTENTION.
+ * SV_ENCODE_UNFUSED_QKV, SV_ENCODE_FP8_ATTENTION and SV_ENCODE_EAGER.
  * Each (batch, gemm_dtype, flags) combination has its own cached workspace.
  * Errors: as sv_encode; unknown flag bits -> SV_ERR_INVALID_ARG.
  */

@@ -160,3 +160,25 @@ def test_27_layers_e4m3_fp8_attention_batch2(sv, so400m, ref27):
     assert cosine_rows(got, ref).min() >= 0.99
     assert np.abs(got - ref).max() <= 0.5
     assert cosine_rows(got, so400m.encode(pix, fp8=True, fp8_attention=True)).min() >= 0.995
+
+
+@pytest.mark.parametrize("dtype,flags", [(0, 0), (1, 2)])
+def test_step_graph_matches_eager_launches(sv, so400m, dtype, flags):
+    """sv_encode launches kernels one by one on the first call with given buffers and
+    options, captures that sequence into a CUDA graph on the second and launches the
+    graph from then on: every call gives the bits of the one-by-one path and counts the
+    same kernels; a new output buffer starts over with a one-by-one call."""
+    B, layers = 2, 2
+    pix = torch.from_numpy(synth.pixels(5, B)).cuda()
+    ref = torch.empty(B, 1, 1152, dtype=torch.float16, device="cuda")
+    sv.sv_launch_count()
+    sv.sv_encode_ex(pix, ref, B, layers, dtype, flags | sv.SV_ENCODE_EAGER)
+    sv.sv_sync()
+    eager_launches = sv.sv_launch_count()
+    for out in (torch.empty_like(ref), torch.empty_like(ref)):
+        for _ in range(4):
+            out.fill_(float("nan"))
+            sv.sv_encode_ex(pix, out, B, layers, dtype, flags)
+            sv.sv_sync()
+            assert sv.sv_launch_count() == eager_launches
+            assert torch.equal(out, ref)

@@ -117,6 +117,7 @@ def sv_model_dims() -> dict:
 
 SV_ENCODE_UNFUSED_QKV = 1
 SV_ENCODE_FP8_ATTENTION = 2
+SV_ENCODE_EAGER = 4
 SV_ATTENTION_QK_E4M3 = 1
 
 

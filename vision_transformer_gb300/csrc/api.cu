@@ -1,6 +1,7 @@
 // C ABI of the library (include/sv.h): resident weights, cached workspaces,
 // the forward-pass orchestration and the per-op entry points. Host code only;
 // every step of the forward pass runs in this library's kernels.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -144,8 +145,32 @@ void* g_lng_scratch = nullptr;  // sv_ln_gemm: scaled weights, column sums, bias
 size_t g_lng_scratch_bytes = 0;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+// Step graphs of sv_encode: one per (pixels, out, batch, layers, dtype, flags) seen at
+// least twice (captured on the second call, replayed from the third on).
+struct StepGraph {
+  const void* pixels = nullptr;
+  const void* out = nullptr;
+  int B = 0, layers = 0, fp8 = 0, flags = 0;
+  int calls = 0;                    // calls so far with this key
+  bool eager_only = false;          // the capture was refused
+  cudaGraphExec_t exec = nullptr;   // the captured launch sequence
+  long long launches = 0;           // kernels in it
+  unsigned long long last_use = 0;  // for eviction
+};
+constexpr size_t kMaxStepGraphs = 8;
+std::vector<StepGraph> g_graphs;
+unsigned long long g_graph_clock = 0;
+cudaStream_t g_capture_stream = nullptr;
+
+void free_graphs() {
+  for (StepGraph& g : g_graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  g_graphs.clear();
+}
+
 
 void free_plans() {
+  free_graphs();  // they launch into the plans' workspaces
   for (auto& kv : g_plans) cudaFree(kv.second->mem);
   for (auto& kv : g_map_plans) cudaFree(kv.second->mem);
   g_plans.clear();
@@ -557,6 +582,64 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
   return run_map(p.map, B, fp8, out, s);
 }
 
+// sv_encode's launches: one by one on the first call with a key (which also creates the
+// workspace, kernel attributes and tensor maps the capture relies on), and whenever
+// profiling or SV_ENCODE_EAGER asks for it; captured into a CUDA graph on an internal
+// stream on the second call; that graph launched on the caller's stream from then on.
+sv_status encode_step(Plan& p, const __half* pixels, __half* out, int layers, int flags, cudaStream_t s) {
+  if (g_prof_on || (flags & SV_ENCODE_EAGER)) return encode(p, pixels, out, layers, s);
+  StepGraph* g = nullptr;
+  for (StepGraph& x : g_graphs)
+    if (x.pixels == pixels && x.out == out && x.B == p.B && x.layers == layers && x.fp8 == p.fp8 && x.flags == flags)
+      g = &x;
+  if (!g) {
+    if (g_graphs.size() >= kMaxStepGraphs) {  // drop the least recently used
+      auto old = std::min_element(g_graphs.begin(), g_graphs.end(), [](const StepGraph& a, const StepGraph& b) {
+        return a.last_use < b.last_use;
+      });
+      if (old->exec) cudaGraphExecDestroy(old->exec);
+      g_graphs.erase(old);
+    }
+    StepGraph n;
+    n.pixels = pixels;
+    n.out = out;
+    n.B = p.B;
+    n.layers = layers;
+    n.fp8 = p.fp8;
+    n.flags = flags;
+    g_graphs.push_back(n);
+    g = &g_graphs.back();
+  }
+  g->last_use = ++g_graph_clock;
+  if (++g->calls == 1 || g->eager_only) return encode(p, pixels, out, layers, s);
+  if (!g->exec) {
+    if (!g_capture_stream)
+      SV_CHECK_CUDA(cudaStreamCreateWithFlags(&g_capture_stream, cudaStreamNonBlocking), "cudaStreamCreate(capture)");
+    SV_CHECK_CUDA(cudaStreamBeginCapture(g_capture_stream, cudaStreamCaptureModeThreadLocal), "cudaStreamBeginCapture");
+    const long long before = g_launches;
+    const sv_status st = encode(p, pixels, out, layers, g_capture_stream);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(g_capture_stream, &graph);
+    const long long n = g_launches - before;
+    g_launches = before;  // counted when the graph is launched
+    cudaGraphExec_t exec = nullptr;
+    cudaError_t ie = cudaErrorUnknown;
+    if (st == SV_OK && ce == cudaSuccess) ie = cudaGraphInstantiate(&exec, graph, 0);
+    if (graph) cudaGraphDestroy(graph);
+    if (st != SV_OK) return st;
+    if (ie != cudaSuccess) {  // capture or instantiation refused: this key runs one by one
+      cudaGetLastError();
+      g->eager_only = true;
+      return encode(p, pixels, out, layers, s);
+    }
+    g->exec = exec;
+    g->launches = n;
+  }
+  SV_CHECK_CUDA(cudaGraphLaunch(g->exec, s), "cudaGraphLaunch(encode step)");
+  g_launches += g->launches;
+  return SV_OK;
+}
+
 sv_status check_ready() {
   if (!g_w.ready) {
     set_error("weights are not initialised: call sv_init_weights first");
@@ -688,7 +771,7 @@ sv_status sv_encode_ex(const void* pixels, void* out, int batch, int layers, int
                        void* stream) {
   SV_TRY(check_ready());
   if (!pixels || !out || batch < 1 || layers < 1 || layers > g_w.d.L ||
-      (gemm_dtype != SV_GEMM_F16 && gemm_dtype != SV_GEMM_E4M3) || (flags & ~(SV_ENCODE_UNFUSED_QKV | SV_ENCODE_FP8_ATTENTION))) {
+      (gemm_dtype != SV_GEMM_F16 && gemm_dtype != SV_GEMM_E4M3) || (flags & ~(SV_ENCODE_UNFUSED_QKV | SV_ENCODE_FP8_ATTENTION | SV_ENCODE_EAGER))) {
     set_error("sv_encode: bad arguments (batch %d, layers %d of %d, gemm_dtype %d, flags %d)", batch, layers,
               g_w.d.L, gemm_dtype, flags);
     return SV_ERR_INVALID_ARG;
@@ -702,9 +785,10 @@ sv_status sv_encode_ex(const void* pixels, void* out, int batch, int layers, int
     return SV_ERR_INVALID_ARG;
   }
   Plan* p = nullptr;
-  SV_TRY(get_plan(batch, gemm_dtype, flags, &p));
-  return encode(*p, static_cast<const __half*>(pixels), static_cast<__half*>(out), layers,
-                static_cast<cudaStream_t>(stream));
+  const int plan_flags = flags & ~SV_ENCODE_EAGER;
+  SV_TRY(get_plan(batch, gemm_dtype, plan_flags, &p));
+  return encode_step(*p, static_cast<const __half*>(pixels), static_cast<__half*>(out), layers,
+                     plan_flags | (flags & SV_ENCODE_EAGER), static_cast<cudaStream_t>(stream));
 }
 
 sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int gemm_dtype, void* stream) {
@@ -1043,6 +1127,8 @@ void sv_shutdown(void) {
   g_prof.clear();
   for (cudaEvent_t e : g_ev_pool) cudaEventDestroy(e);
   g_ev_pool.clear();
+  if (g_capture_stream) cudaStreamDestroy(g_capture_stream);
+  g_capture_stream = nullptr;
   if (g_rt.dev_err) cudaFree(g_rt.dev_err);
   g_rt = Runtime();
 }
