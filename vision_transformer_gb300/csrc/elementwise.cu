@@ -303,37 +303,76 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, int* err) {
   }
 }
 
-// LayerNorm statistics from a GEMM epilogue's per-tile partials, one thread per row:
-// each tile has two partials, over its 32-column chunks c = 0, 2, ... and c = 1, 3, ...
-// (a partial covering no column is absent). Their (count, mean, M2) are merged left to
-// right with the pairwise update of
-// Chan, Golub and LeVeque (1979): n = na + nb, d = mean_b - mean_a,
-// mean = mean_a + d nb / n, M2 = M2a + M2b + d^2 na nb / n; then var = M2 / width
-// (biased, as the LayerNorm kernel) and the same r / aug outputs as its statistics mode.
+// LayerNorm statistics from a GEMM epilogue's per-tile partials: each tile has two
+// partials, over its 32-column chunks c = 0, 2, ... and c = 1, 3, ... (a partial
+// covering no column is absent). kLanes consecutive lanes share a row: 8 for few rows
+// (lane j loads the row's partials j, j + 8, ..., all before any arithmetic, so a row's
+// loads are in flight together), 1 for many (a thread walks its row's partials in order;
+// the other rows' threads hide the latency, and more lanes would only add arithmetic).
+// A lane merges its partials, and the lanes' results are merged by shuffles,
+// each merge being the pairwise update of Chan, Golub and LeVeque (1979): n = na + nb,
+// d = mean_b - mean_a, mean = mean_a + d nb / n, M2 = M2a + M2b + d^2 na nb / n. Then
+// var = M2 / width (biased, as the LayerNorm kernel) and the same r / aug outputs as its
+// statistics mode.
+
+// (n, mean, m2) <- merge with (nb, mb, m2b); a side with no columns leaves the other.
+__device__ __forceinline__ void chan_merge(float& n, float& mean, float& m2, float nb, float mb, float m2b) {
+  if (nb == 0.0f) return;
+  const float nn = n + nb, d = mb - mean, f = __fdividef(nb, nn);
+  mean = fmaf(d, f, mean);
+  m2 += m2b + d * d * (n * f);
+  n = nn;
+}
+
+template <int kLanes>
 __global__ void __launch_bounds__(128) ln_finalize_kernel(const float2* __restrict__ part, int tiles, int tile_w,
                                                          float* __restrict__ r, __half* __restrict__ aug,
                                                          int rows, int width, float eps) {
+  constexpr int kPerLane = (kMaxLnTiles + kLanes - 1) / kLanes;  // partials one lane may hold
   pdl_launch_dependents();
   pdl_wait();
-  const int row = int(blockIdx.x) * 128 + int(threadIdx.x);
-  if (row >= rows) return;
-  const float2* pr = part + size_t(row) * size_t(2 * tiles);
+  const int gt = int(blockIdx.x) * 128 + int(threadIdx.x);
+  const int row = gt / kLanes, j = gt % kLanes;
+  const bool live = row < rows;
+  const int entries = 2 * tiles;
+  const float2* pr = part + size_t(live ? row : 0) * size_t(entries);
   float n = 0.0f, mean = 0.0f, m2 = 0.0f;
-  for (int t = 0; t < tiles; ++t) {
+  // columns of chunks h, h + 2, ... of tile t (the last chunk may be partial)
+  auto cols_of = [&](int t, int h) {
     const int w = min(tile_w, width - t * tile_w), chunks = (w + 31) / 32, last = w - 32 * (chunks - 1);
+    return 32 * ((chunks - h + 1) / 2) - (((chunks - 1) & 1) == h ? 32 - last : 0);
+  };
+  if constexpr (kLanes == 1) {
+    if (live)
+      for (int e = 0; e < entries; ++e) {
+        const int cols = cols_of(e >> 1, e & 1);
+        if (cols > 0) {
+          const float2 q = __ldg(pr + e);
+          chan_merge(n, mean, m2, float(cols), q.x, q.y);
+        }
+      }
+  } else {
+    float2 q[kPerLane];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      // columns of chunks h, h + 2, ... (the last chunk may be partial)
-      const int cols = 32 * ((chunks - h + 1) / 2) - (((chunks - 1) & 1) == h ? 32 - last : 0);
-      if (cols <= 0) continue;
-      const float nb = float(cols);
-      const float2 q = __ldg(pr + 2 * t + h);
-      const float nn = n + nb, d = q.x - mean, f = __fdividef(nb, nn);
-      mean = fmaf(d, f, mean);
-      m2 += q.y + d * d * (n * f);
-      n = nn;
+    for (int i = 0; i < kPerLane; ++i) {
+      const int e = j + i * kLanes;
+      q[i] = (live && e < entries) ? __ldg(pr + e) : make_float2(0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+      const int e = j + i * kLanes;
+      if (!live || e >= entries) break;
+      const int cols = cols_of(e >> 1, e & 1);
+      if (cols > 0) chan_merge(n, mean, m2, float(cols), q[i].x, q[i].y);
+    }
+#pragma unroll
+    for (int o = 1; o < kLanes; o <<= 1) {
+      const float nb = __shfl_xor_sync(0xffffffffu, n, o), mb = __shfl_xor_sync(0xffffffffu, mean, o),
+                  m2b = __shfl_xor_sync(0xffffffffu, m2, o);
+      chan_merge(n, mean, m2, nb, mb, m2b);
     }
   }
+  if (!live || j != 0) return;
   const float rstd = rsqrtf(m2 / float(width) + eps);
   const __half hi = __float2half_rn(-mean);
   const __half lo = __float2half_rn(-mean - __half2float(hi));
@@ -429,8 +468,17 @@ sv_status ln_stats_launch(const __half* x, float* stats_r, __half* stats_aug, in
 
 sv_status ln_finalize_launch(const float2* part, int tiles, int tile_w, float* r, __half* aug, int rows, int width,
                              float eps, cudaStream_t s) {
-  cudaError_t e = launch_pdl(ln_finalize_kernel, dim3(unsigned((rows + 127) / 128)), dim3(128), 0, s, part, tiles, tile_w,
-                             r, aug, rows, width, eps);
+  if (tiles < 1 || 2 * tiles > kMaxLnTiles) {
+    set_error("ln_finalize: %d column tiles (at most %d)", tiles, kMaxLnTiles / 2);
+    return SV_ERR_UNSUPPORTED;
+  }
+  const bool few = rows < 16384;
+  const long threads = long(rows) * (few ? 8 : 1);
+  const dim3 grid(unsigned((threads + 127) / 128));
+  cudaError_t e = few ? launch_pdl(ln_finalize_kernel<8>, grid, dim3(128), 0, s, part, tiles, tile_w, r, aug, rows,
+                                   width, eps)
+                      : launch_pdl(ln_finalize_kernel<1>, grid, dim3(128), 0, s, part, tiles, tile_w, r, aug, rows,
+                                   width, eps);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "ln_finalize launch");
 }
 
