@@ -182,3 +182,44 @@ def test_step_graph_matches_eager_launches(sv, so400m, dtype, flags):
             sv.sv_sync()
             assert sv.sv_launch_count() == eager_launches
             assert torch.equal(out, ref)
+
+
+def test_step_graphs_follow_weights_and_eviction(sv):
+    """Step graphs hold the workspaces and weights of the call that captured them:
+    re-initialising the weights drops them (the same buffers then give the new
+    weights' result), and more argument sets than the cache keeps are evicted and
+    re-captured without changing any result."""
+    B, layers = 1, 1
+    pix = torch.from_numpy(synth.pixels(7, B)).cuda()
+
+    def eager(seed):
+        sv.sv_init_weights(seed)
+        ref = torch.empty(B, 1, 1152, dtype=torch.float16, device="cuda")
+        sv.sv_encode_ex(pix, ref, B, layers, 0, sv.SV_ENCODE_EAGER)
+        sv.sv_sync()
+        return ref
+
+    ref1 = eager(1)
+    ref0 = eager(0)
+    assert not torch.equal(ref0, ref1)
+    out = torch.empty_like(ref0)
+    for _ in range(3):  # one by one, captured, replayed
+        sv.sv_encode(pix, out, B, layers, 0)
+    sv.sv_sync()
+    assert torch.equal(out, ref0)
+    sv.sv_init_weights(1)
+    for _ in range(3):
+        out.zero_()
+        sv.sv_encode(pix, out, B, layers, 0)
+        sv.sv_sync()
+        assert torch.equal(out, ref1)
+    # twelve output buffers in turn, three rounds: more keys than the cache holds
+    outs = [torch.empty_like(ref1) for _ in range(12)]
+    for _ in range(3):
+        for o in outs:
+            o.zero_()
+            sv.sv_encode(pix, o, B, layers, 0)
+        sv.sv_sync()
+        for o in outs:
+            assert torch.equal(o, ref1)
+    sv.sv_init_weights(0)  # leave the module's weights as the fixtures expect
