@@ -113,7 +113,8 @@ sv_status sv_model_dims(int* tokens, int* patch_dim, int* width, int* heads, int
  * identical results. The graphs name the caller's buffers by address, so a
  * buffer freed and reallocated at the same address must keep its role; the
  * graphs are dropped by sv_init_weights and sv_shutdown. Calls made while
- * profiling is on (sv_profile_enable) always launch one by one.
+ * profiling is on (sv_profile_enable), or on a stream the caller is capturing
+ * into a graph of its own, launch one by one.
  * Errors: SV_ERR_NOT_INITIALIZED, SV_ERR_INVALID_ARG, SV_ERR_OOM, SV_ERR_CUDA.
  */
 sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int gemm_dtype, void* stream);

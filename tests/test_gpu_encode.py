@@ -223,3 +223,27 @@ def test_step_graphs_follow_weights_and_eviction(sv):
         for o in outs:
             assert torch.equal(o, ref1)
     sv.sv_init_weights(0)  # leave the module's weights as the fixtures expect
+
+
+def test_encode_inside_a_caller_graph(sv, so400m):
+    """A caller that captures sv_encode into a CUDA graph of its own (here with torch)
+    records the kernels themselves, also for arguments whose step graph the library
+    already holds; replaying the caller's graph gives the one-by-one result."""
+    B, layers = 1, 1
+    pix = torch.from_numpy(synth.pixels(9, B)).cuda()
+    ref = torch.empty(B, 1, 1152, dtype=torch.float16, device="cuda")
+    sv.sv_encode_ex(pix, ref, B, layers, 0, sv.SV_ENCODE_EAGER)
+    sv.sv_sync()
+    out = torch.empty_like(ref)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        for _ in range(3):  # one by one, captured by the library, replayed
+            sv.sv_encode(pix, out, B, layers, 0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        sv.sv_encode(pix, out, B, layers, 0)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)

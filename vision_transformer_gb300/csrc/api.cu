@@ -588,6 +588,12 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
 // stream on the second call; that graph launched on the caller's stream from then on.
 sv_status encode_step(Plan& p, const __half* pixels, __half* out, int layers, int flags, cudaStream_t s) {
   if (g_prof_on || (flags & SV_ENCODE_EAGER)) return encode(p, pixels, out, layers, s);
+  // a caller capturing its own stream records the kernels themselves
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return encode(p, pixels, out, layers, s);
+  }
   StepGraph* g = nullptr;
   for (StepGraph& x : g_graphs)
     if (x.pixels == pixels && x.out == out && x.B == p.B && x.layers == layers && x.fp8 == p.fp8 && x.flags == flags)
