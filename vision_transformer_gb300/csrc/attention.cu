@@ -617,12 +617,10 @@ __global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restric
   *reinterpret_cast<uint4*>(dst + cg * kGroupBytes) = u;
 }
 
-// Buffer configuration: 0 = two Q buffers, 2 + 2 K / V stages; 1 = one Q buffer,
-// 3 + 3 stages; 2 = one Q buffer, 4 K + 2 V stages. All three fill the same shared
-// memory; 1 measured fastest at 16 heads x 729 tokens (B = 32: 137 / 139 / 139 us).
-int g_attention_config = 1;
-int attention_config() { return g_attention_config; }
-
+// Buffer configuration launched: one Q buffer (both tiles of an item) and 3 + 3 K / V
+// stages. Two Q buffers with 2 + 2 stages, or one with 4 K + 2 V stages, fill the same
+// shared memory and measured slower at 16 heads x 729 tokens (B = 32: 137 us against
+// 139 and 139 us).
 template <int QB, int KS, int VS, bool QK8>
 sv_status attention_launch_cfg(const CUtensorMap& tmo, const Params& p, int grid, cudaStream_t s) {
   static bool attr_set = false;
@@ -679,11 +677,7 @@ sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, fl
     if (st != SV_OK) return st;
   }
   if (qk8) return attention_launch_cfg<1, 3, 3, true>(tmo, p, grid, s);
-  switch (attention_config()) {
-    case 1: return attention_launch_cfg<1, 3, 3, false>(tmo, p, grid, s);
-    case 2: return attention_launch_cfg<1, 4, 2, false>(tmo, p, grid, s);
-    default: return attention_launch_cfg<2, 2, 2, false>(tmo, p, grid, s);
-  }
+  return attention_launch_cfg<1, 3, 3, false>(tmo, p, grid, s);
 }
 
 }  // namespace sv
