@@ -5,6 +5,8 @@ Configurations (the pages' workloads; weights and pixels from synth/):
     the four-token full-width diagnostic ("SigLIP ViT benchmark");
   - one So400m/14 layer + MAP at batch 1 and batch 8, F16 GEMMs;
   - 27 layers + MAP at batch 1, F16 GEMMs;
+  - 27 layers + MAP at batch 128 (the throughput workload), F16 and E4M3 GEMMs,
+    on sampled images;
   - 27 layers + MAP at batch 2 with E4M3 GEMM operands at scale 2^-4, against
     the unquantised oracle (and the oracle's operand-rounding mode), also with
     the FP8 attention products (Q and K in E4M3).
@@ -160,6 +162,28 @@ def test_27_layers_e4m3_fp8_attention_batch2(sv, so400m, ref27):
     assert cosine_rows(got, ref).min() >= 0.99
     assert np.abs(got - ref).max() <= 0.5
     assert cosine_rows(got, so400m.encode(pix, fp8=True, fp8_attention=True)).min() >= 0.995
+
+
+@pytest.fixture(scope="module")
+def ref27_b128(so400m):
+    pix = synth.pixels(11, 128)
+    idx = [0, 127]  # the first image and the last (the row tail of every GEMM)
+    return pix, idx, so400m.encode(pix[idx])
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_27_layers_batch128_sampled(sv, ref27_b128, dtype):
+    """The throughput workload in its own launch configuration (27 layers + MAP at
+    batch 128: the tile schedules, the one-thread-per-row statistics merge and the
+    attention grid of that size): sampled images against the oracle, which computes
+    them one by one (images are independent), at the 27-layer bounds."""
+    pix, idx, ref = ref27_b128
+    got = _encode(sv, pix, 27, dtype)[idx]
+    if dtype == 0:
+        assert cosine_rows(got, ref).min() >= 0.995
+    else:
+        assert cosine_rows(got, ref).min() >= 0.99
+        assert np.abs(got - ref).max() <= 0.5
 
 
 @pytest.mark.parametrize("dtype,flags", [(0, 0), (1, 2)])
