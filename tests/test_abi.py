@@ -50,6 +50,16 @@ def test_binding_covers_exactly_the_header():
         assert callable(getattr(vt, n))
 
 
+def test_binding_constants_match_the_header():
+    """Every enumerator include/sv.h defines has the same value in the binding."""
+    import vision_transformer_gb300 as vt
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    values = dict((n, int(v)) for n, v in re.findall(r"\b(SV_[A-Z0-9_]+)\s*=\s*(\d+)", text))
+    assert len(values) >= 17
+    for name, value in values.items():
+        assert getattr(vt, name) == value, name
+
+
 def test_errors_before_device_work(lib):
     """Bad arguments are rejected on the host, so these calls need no GPU."""
     import vision_transformer_gb300 as vt
