@@ -143,7 +143,8 @@ typedef enum {
 /*
  * sv_encode with options: flags is 0 (exactly sv_encode) or any OR of
  * SV_ENCODE_UNFUSED_QKV, SV_ENCODE_FP8_ATTENTION and SV_ENCODE_EAGER.
- * Each (batch, gemm_dtype, flags) combination has its own cached workspace.
+ * Each (batch, gemm_dtype, flags without SV_ENCODE_EAGER) combination has its
+ * own cached workspace.
  * Errors: as sv_encode; unknown flag bits -> SV_ERR_INVALID_ARG.
  */
 sv_status sv_encode_ex(const void* pixels, void* out, int batch, int layers, int gemm_dtype, int flags,
