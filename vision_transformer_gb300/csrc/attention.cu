@@ -32,23 +32,31 @@
 //   - query rows past the last token are computed but never stored.
 //
 // Persistent CTAs (one per SM) walk work items of (256 queries as two 128-row
-// tiles, head, image); 352 threads:
-//   warp 0      bulk copies: Q (both tiles) per item, then K and V tiles of 128
-//               keys into 3 + 3 stages, each with its own release;
-//   warps 1, 2  MMA issuers, one per softmax group w: S_w = Q_w K_j^T
-//               (M 128, N 128) into TMEM, then O_w += P_w V_j (M 128, N 80) in
-//               two 64-key halves, O_w kept in TMEM for the whole item;
-//   warps 3..6  softmax group 0, warps 7..10 softmax group 1: one thread per
-//               query row reads its S row from TMEM once (S is then free for the
-//               next product), writes P (F16) to shared memory, and rescales O
-//               in TMEM only when the row maximum grows by more than 2^15; the
-//               softmax denominator comes out of the P V product (a column of
-//               ones in V's pad group). An item's output rows are staged in shared
-//               memory and written by a TMA store during the next item.
+// tiles, head, image); 320 threads:
+//   warp 0      bulk copies: Q (both tiles) of the next item into a staging buffer,
+//               K and V tiles of 128 keys into 3 + 3 stages, each with its own release;
+//   warp 1      the MMA issuer, in the order S_0(0), S_1(0), then per key tile t:
+//               O_0 += P_0(t) V_t, S_0(t+1), O_1 += P_1(t) V_t, S_1(t+1), where
+//               S_w = Q_w K^T (M 128, N 128) and O_w += P_w V (M 128, N 80). Q_w and
+//               P_w are read from tensor memory, only K and V from shared memory. The
+//               MMAs of one thread run in issue order, so S_w(t+1) overwrites P_w(t)
+//               only after the P V product has read it, and the completion of S_w(t+1)
+//               also means that O_w holds the sum up to tile t. One issuer for both
+//               groups staggers them: group 1's products run while group 0 computes
+//               its softmax, and the other way round;
+//   warps 2..5  softmax group 0, warps 6..9 softmax group 1: one thread per query
+//               row reads its S row from TMEM, writes P = 2^(scale s - m) as F16
+//               pairs back over the first 64 columns of S, and rescales O in TMEM
+//               only when the row maximum grows by more than 2^15; the softmax
+//               denominator comes out of the P V product (a column of ones in V's
+//               pad group). On an item's last tile the group also moves the next
+//               item's Q rows from the staging buffer into TMEM; an item's output rows
+//               are written from registers at the start of the group's next item.
+// Shared-memory traffic per key tile is then the K and V copies and their reads by
+// the tensor core: an N = 80 or N = 128 product with both operands in shared memory
+// needs about as many bytes per cycle as shared memory delivers.
 
 #include <cuda_fp8.h>
-
-#include <cstring>
 
 #include "ptx.cuh"
 #include "sv_internal.h"
@@ -66,11 +74,10 @@ constexpr int kOpBytes = 10 * kGroupBytes;   // 80 columns in shared memory (72 
 // 8 zero bytes), 6 in shared memory (96 columns: three MMA K steps of 32)
 constexpr int kGroups8 = 5;
 constexpr int kOpBytes8 = 6 * kGroupBytes;
-constexpr int kPBytes = 16 * kGroupBytes;    // 128 keys of probabilities
-constexpr int kThreads = 352;
+constexpr int kThreads = 320;
 constexpr int kBarBytes = 384;  // barriers, TMEM address slot, abort flag
 
-// Shared memory map (offsets from the 1024-aligned base) for QB query buffers
+// Shared memory map (offsets from the 1024-aligned base) for QB query staging buffers
 // (of two tiles each), KS key stages and VS value stages; QK8: E4M3 Q and K tiles.
 template <int QB, int KS, int VS, bool QK8>
 struct Smem {
@@ -78,14 +85,14 @@ struct Smem {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * QB * kQKOp;
   static constexpr int kOffV = kOffK + KS * kQKOp;
-  static constexpr int kOffP = kOffV + VS * kOpBytes;  // one buffer per softmax group
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffV + VS * kOpBytes;
   static constexpr int kBytes = 1024 + kOffBar + kBarBytes;
   static_assert(kBytes <= 232448, "shared memory budget");
   static_assert(QB >= 1 && QB <= 2 && KS >= 2 && KS <= 4 && VS >= 2 && VS <= 4, "buffer counts");
 };
 
-// TMEM columns: S_w at 128 w, O_w at 256 + 128 w.
+// TMEM columns: S_w at 128 w (P_w, 64 columns of F16 pairs, over its first half), O_w
+// at 256 + 80 w, Q_w at 416 + 48 w (40 columns of F16 pairs, or 24 of E4M3 quads).
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
@@ -100,20 +107,17 @@ struct Params {
 // Barrier indices (8 bytes each).
 enum {
   kBarQFull = 0,    // +buffer
-  kBarQEmpty = 2,   // +buffer: both groups' last S product of the item has finished
+  kBarQEmpty = 2,   // +buffer: every softmax thread has moved its Q row into TMEM
   kBarKFull = 4,    // +stage
   kBarKEmpty = 8,   // +stage
   kBarVFull = 12,   // +stage
   kBarVEmpty = 16,  // +stage
-  kBarSFull = 20,   // +group
-  kBarSEmpty = 22,  // +group: the group has read S into registers
-  kBarPFull = 24,   // +2 group + half: that half of the group's P tile is written
-  kBarPEmpty = 28,  // +2 group + half: O += P V of that half has finished
-  kBarOFull = 32,   // +group: O += P V of the group's latest tile has finished
-  kBarOEmpty = 34,  // +group: the group has read the item's final O
-  kBarDrain = 36,   // +group
-  kBarStage = 38,   // +group: every warp's output store has read its staging rows
-  kNumBars = 40
+  kBarSFull = 20,   // +group: S_w(t) has finished (and with it O_w += P_w(t-1) V_{t-1})
+  kBarPFull = 22,   // +group: the group has written P_w(t) (and any O rescale, and on an
+                    //   item's last tile the next item's Q) to TMEM
+  kBarQtFull = 24,  // +group: the first item's Q rows are in TMEM
+  kBarDrain = 26,
+  kNumBars = 27
 };
 static_assert(8 * kNumBars + 8 <= kBarBytes, "barrier area");
 
@@ -183,15 +187,15 @@ __device__ __forceinline__ Item item_of(int it, int nq, int H) {
 }
 
 // Persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...
-// The K / V stream and the softmax pipeline run on across item boundaries; Q is
-// double buffered so the next item's queries arrive during the current item.
+// The K / V stream and the softmax pipeline run on across item boundaries; the next
+// item's Q arrives in the staging buffer while the current item runs.
 template <int QB, int KS, int VS, bool QK8>
-// 11 warps: three share each of three SM sub-partitions, so a thread may hold at most
+// 10 warps: three share each of two SM sub-partitions, so a thread may hold at most
 // 16384 / (3 x 32) registers, rounded down to the allocation granule.
-__global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtensorMap tm_out, const Params p) {
+__global__ void __maxnreg__(168) attention_kernel(const Params p) {
   using L = Smem<QB, KS, VS, QK8>;
   constexpr int kQKOp = L::kQKOp, kQKGroups = QK8 ? kGroups8 : kGroups;
-  constexpr int kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffP = L::kOffP, kOffBar = L::kOffBar;
+  constexpr int kOffQ = L::kOffQ, kOffK = L::kOffK, kOffV = L::kOffV, kOffBar = L::kOffBar;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -215,7 +219,7 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
   // Zero every operand buffer (Q, K and V tiles including their pad column group),
   // except V's pad group, whose first column is 1: P V then carries the row sum
   // of P (the softmax denominator, from the same F16 P) in output column 72.
-  for (int i = threadIdx.x; i < kOffP / 16; i += kThreads) {
+  for (int i = threadIdx.x; i < kOffBar / 16; i += kThreads) {
     const int off = i * 16;
     const bool v_pad = off >= kOffV && ((off - kOffV) % kOpBytes) >= kGroups * kGroupBytes;
     reinterpret_cast<uint4*>(smem)[i] = make_uint4(v_pad ? 0x3C00u : 0u, 0, 0, 0);
@@ -224,30 +228,22 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
   if (threadIdx.x == 0) {
     for (int s = 0; s < QB; ++s) {
       mbar_init(bar(kBarQFull + s), 1);
-      mbar_init(bar(kBarQEmpty + s), 2);  // one release per group
+      mbar_init(bar(kBarQEmpty + s), 256);  // every softmax thread
     }
     for (int s = 0; s < KS; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
-      mbar_init(bar(kBarKEmpty + s), 2);
+      mbar_init(bar(kBarKEmpty + s), 1);
     }
     for (int s = 0; s < VS; ++s) {
       mbar_init(bar(kBarVFull + s), 1);
-      mbar_init(bar(kBarVEmpty + s), 2);
+      mbar_init(bar(kBarVEmpty + s), 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(kBarSFull + w), 1);
-      mbar_init(bar(kBarSEmpty + w), 128);  // every softmax thread of the group arrives
-      for (int h = 0; h < 2; ++h) {
-        mbar_init(bar(kBarPFull + 2 * w + h), 128);
-        mbar_init(bar(kBarPEmpty + 2 * w + h), 1);
-      }
-      mbar_init(bar(kBarOFull + w), 1);
-      mbar_init(bar(kBarOEmpty + w), 128);
+      mbar_init(bar(kBarPFull + w), 128);  // every softmax thread of the group arrives
+      mbar_init(bar(kBarQtFull + w), 128);
     }
     mbar_init(bar(kBarDrain), 1);
-    mbar_init(bar(kBarDrain + 1), 1);
-    mbar_init(bar(kBarStage), 4);  // one arrival per warp of the group
-    mbar_init(bar(kBarStage + 1), 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -311,90 +307,119 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
         if (issued & (1u << i)) mbar_wait_bounded(bar(fb), (issued_phase >> i) & 1, p.err);
       }
     }
-  } else if (warp <= 2) {
+  } else if (warp == 1) {
     if (lane == 0) {
-      // MMA issuer of softmax group w = warp - 1, in the group's own order: S(0); then per
-      // tile t (item t / nkv, key tile t % nkv): S(t+1) once K_{t+1} (and, on an item's
-      // first tile, its Q) is in and the group has read S(t) from TMEM; O += P V for
-      // each 64-key half of P(t) once that half is written, V_t is in and (an item's
-      // first tile) the group has read the previous item's O.
-      const int w = warp - 1;
-      // S = Q K^T, both K-major (F16, or E4M3 with the same type code 0 under kind::f8f6f4)
+      // The MMA issuer. Tile t = item t / nkv, key tile t % nkv. After the last tile one
+      // more commit on each group's S barrier tells the group that its O is final.
+      // S = Q K^T with A (Q) in TMEM and B (K) K-major in shared memory (F16, or E4M3
+      // with the same type code 0 under kind::f8f6f4); O = P V with A (P) in TMEM and B
+      // (V) MN-major in shared memory.
       constexpr uint32_t idesc_s = make_idesc(128, 128, 0, false);
-      constexpr uint32_t idesc_o = make_idesc(128, 80, 0, true);    // O = P V, V MN-major
-      auto issue_s = [&](int t) -> bool {
-        const int n = t / nkv, j = t - n * nkv;
-        if (!mbar_wait(bar(kBarKFull + t % KS), (t / KS) & 1, abort_flag, p.err)) return false;
-        if (!mbar_wait(bar(kBarSEmpty + w), (t & 1) ^ 1, abort_flag, p.err)) return false;
-        if (j == 0 && !mbar_wait(bar(kBarQFull + n % QB), (n / QB) & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const uint32_t qa = sbase + kOffQ + (2 * (n % QB) + w) * kQKOp, ka = sbase + kOffK + (t % KS) * kQKOp;
+      constexpr uint32_t idesc_o = make_idesc(128, 80, 0, true);
+      auto issue_s = [&](int w, int t) {
+        const uint32_t s_tm = tmem + uint32_t(128 * w), q_tm = tmem + uint32_t(416 + 48 * w);
+        const uint32_t ka = sbase + kOffK + (t % KS) * kQKOp;
         if (QK8) {
 #pragma unroll
           for (int kk = 0; kk < 3; ++kk)  // K = 96 in steps of 32 (two 16-byte column groups)
-            mma_f8(tmem + uint32_t(w * 128), make_sdesc(qa + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
-                   make_sdesc(ka + kk * 2 * kGroupBytes, kGroupBytes, 128, 0), idesc_s, kk > 0);
+            mma_f8_ts(s_tm, q_tm + uint32_t(8 * kk), make_sdesc(ka + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
+                      idesc_s, kk > 0);
         } else {
 #pragma unroll
           for (int kk = 0; kk < 5; ++kk)  // K = 80 in steps of 16 (two column groups)
-            mma_f16(tmem + uint32_t(w * 128), make_sdesc(qa + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
-                    make_sdesc(ka + kk * 2 * kGroupBytes, kGroupBytes, 128, 0), idesc_s, kk > 0);
+            mma_f16_ts(s_tm, q_tm + uint32_t(8 * kk), make_sdesc(ka + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
+                       idesc_s, kk > 0);
         }
         tc_commit(bar(kBarSFull + w));
-        tc_commit(bar(kBarKEmpty + t % KS));
-        if (j == nkv - 1) tc_commit(bar(kBarQEmpty + n % QB));
-        return true;
       };
-      auto issue_pv = [&](int u, int half) -> bool {
-        const int n = u / nkv, j = u - n * nkv;
-        if (!mbar_wait(bar(kBarPFull + 2 * w + half), u & 1, abort_flag, p.err)) return false;
-        if (!mbar_wait(bar(kBarVFull + u % VS), (u / VS) & 1, abort_flag, p.err)) return false;
-        if (j == 0 && half == 0 && n > 0 && !mbar_wait(bar(kBarOEmpty + w), (n - 1) & 1, abort_flag, p.err))
-          return false;
-        tc_fence_after();
-        const uint32_t pa = sbase + kOffP + w * kPBytes + half * (kPBytes / 2),
-                       va = sbase + kOffV + (u % VS) * kOpBytes + half * 4 * 256;
+      auto issue_pv = [&](int w, int t) {
+        const uint32_t s_tm = tmem + uint32_t(128 * w), o_tm = tmem + uint32_t(256 + 80 * w);
+        const uint32_t va = sbase + kOffV + (t % VS) * kOpBytes;
+        const int j = t % nkv;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // K = 64 keys in steps of 16
-          mma_f16(tmem + uint32_t(256 + w * 128), make_sdesc(pa + kk * 2 * kGroupBytes, kGroupBytes, 128, 0),
-                  make_sdesc(va + kk * 256, 128, kGroupBytes, 0), idesc_o, (j | half | kk) > 0);
-        tc_commit(bar(kBarPEmpty + 2 * w + half));
-        if (half) {
-          tc_commit(bar(kBarOFull + w));
-          tc_commit(bar(kBarVEmpty + u % VS));
-        }
-        return true;
+        for (int kk = 0; kk < 8; ++kk)  // K = 128 keys in steps of 16 (8 TMEM columns of P each)
+          mma_f16_ts(o_tm, s_tm + uint32_t(8 * kk), make_sdesc(va + kk * 256, 128, kGroupBytes, 0), idesc_o,
+                     (j | kk) > 0);
       };
-      bool ok = total == 0 || issue_s(0);
-      for (int t = 0; ok && t < total; ++t)
-        ok = (t + 1 >= total || issue_s(t + 1)) && issue_pv(t, 0) && issue_pv(t, 1);
-      tc_commit(bar(kBarDrain + w));
-      mbar_wait_bounded(bar(kBarDrain + w), 0, p.err);
+      bool ok = total > 0;
+      if (ok) {
+        ok = mbar_wait(bar(kBarKFull), 0, abort_flag, p.err);
+        for (int w = 0; w < 2 && ok; ++w) {
+          ok = mbar_wait(bar(kBarQtFull + w), 0, abort_flag, p.err);
+          if (ok) {
+            tc_fence_after();
+            issue_s(w, 0);
+          }
+        }
+        if (ok) tc_commit(bar(kBarKEmpty));
+      }
+      for (int t = 0; ok && t < total; ++t) {
+        for (int w = 0; w < 2 && ok; ++w) {
+          ok = mbar_wait(bar(kBarPFull + w), t & 1, abort_flag, p.err) &&
+               (w == 1 || mbar_wait(bar(kBarVFull + t % VS), (t / VS) & 1, abort_flag, p.err));
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(w, t);
+          if (w == 1) tc_commit(bar(kBarVEmpty + t % VS));
+          if (t + 1 < total) {
+            const int u = t + 1;
+            if (w == 0 && !(ok = mbar_wait(bar(kBarKFull + u % KS), (u / KS) & 1, abort_flag, p.err))) break;
+            tc_fence_after();
+            issue_s(w, u);
+            if (w == 1) tc_commit(bar(kBarKEmpty + u % KS));
+          } else {
+            tc_commit(bar(kBarSFull + w));  // O_w final
+          }
+        }
+      }
+      tc_commit(bar(kBarDrain));
+      mbar_wait_bounded(bar(kBarDrain), 0, p.err);
     }
   } else {
-    const int w = (warp - 3) >> 2;  // softmax group
+    const int w = (warp - 2) >> 2;  // softmax group
     const int sub = warp & 3;       // TMEM lane quarter
     const int r = sub * 32 + lane;  // query row within the group's tile == TMEM lane
     const uint32_t lane_off = uint32_t(sub * 32) << 16;
     const uint32_t s_tm = tmem + uint32_t(w * 128) + lane_off;
-    const uint32_t o_tm = tmem + uint32_t(256 + w * 128) + lane_off;
-    uint8_t* pbuf = smem + kOffP + w * kPBytes;
+    const uint32_t o_tm = tmem + uint32_t(256 + w * 80) + lane_off;
+    const uint32_t q_tm = tmem + uint32_t(416 + w * 48) + lane_off;
     const float sl2 = QK8 ? p.scale_log2 * (1.0f / 256.0f) : p.scale_log2;  // E4M3 operands hold 16 q, 16 k
     const int D = p.H * kDh;
-    // An item's output rows, at the end of its last tile (the S row is no longer held,
-    // so all 80 columns of O are read at once): the final O (with its row sum in column
-    // 72) of the group's query tile, read from TMEM once its last P V has finished,
-    // scaled by 1 / row sum. F16 rows are staged as this warp's 32 x 72 block in the
-    // group's P buffer (free once that P V has finished) and written by one TMA store
-    // that clips the rows past the image's last token; E4M3 rows are stored directly.
-    auto finish_item = [&](int n, int tl) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), tl & 1, abort_flag, p.err))) return false;
-      tc_fence_after();
+    // Q row r of the group's tile of item n: from the staging buffer into TMEM (F16
+    // pairs, 40 columns with the zero pad; or E4M3 quads, 24 columns), then the buffer
+    // is released to the copy warp.
+    auto stage_q = [&](int n) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarQFull + n % QB), (n / QB) & 1, abort_flag, p.err)))
+        return false;
+      const uint8_t* qs = smem + kOffQ + (2 * (n % QB) + w) * kQKOp + r * 16;
+      if (QK8) {
+        uint32_t q[16], z[8];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(&q[4 * g]) = *reinterpret_cast<const uint4*>(qs + g * kGroupBytes);
+        const uint4 last = *reinterpret_cast<const uint4*>(qs + 4 * kGroupBytes);
+        z[0] = last.x, z[1] = last.y, z[2] = last.z, z[3] = last.w;
+        z[4] = z[5] = z[6] = z[7] = 0u;
+        tmem_st16(q_tm, q);
+        tmem_st8(q_tm + 16, z);
+      } else {
+        uint32_t q[32], z[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) *reinterpret_cast<uint4*>(&q[4 * g]) = *reinterpret_cast<const uint4*>(qs + g * kGroupBytes);
+        const uint4 last = *reinterpret_cast<const uint4*>(qs + 8 * kGroupBytes);
+        z[0] = last.x, z[1] = last.y, z[2] = last.z, z[3] = last.w;
+        z[4] = z[5] = z[6] = z[7] = 0u;
+        tmem_st32(q_tm, q);
+        tmem_st8(q_tm + 32, z);
+      }
+      mbar_arrive(bar(kBarQEmpty + n % QB));
+      return true;
+    };
+    // Output rows of item n, once its last P V has finished: O (with its row sum in
+    // column 72) read from TMEM, scaled by 1 / row sum, stored as F16 (16-byte stores)
+    // or E4M3 codes of 16 x (8-byte stores); rows past the image's last token are not stored.
+    auto write_item = [&](int n) {
       const Item I = item_of(int(blockIdx.x) + n * int(gridDim.x), nq, p.H);
-      const int tq0 = (2 * I.qp + w) * kTile + sub * 32;  // first query row of this warp
-      const int tq = tq0 + lane;
-      uint8_t* stg = pbuf + sub * (32 * kDh * 2) + lane * (kDh * 2);
-      uint8_t* dst8 = static_cast<uint8_t*>(p.out) + (size_t(I.b) * size_t(T) + size_t(tq)) * size_t(D) + size_t(I.h) * kDh;
+      const int tq = (2 * I.qp + w) * kTile + r;
       uint32_t o[5][16];
 #pragma unroll
       for (int c = 0; c < 5; ++c) tmem_ld16(o_tm + 16 * c, o[c]);
@@ -403,7 +428,9 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
       for (int c = 0; c < 5; ++c)
 #pragma unroll
         for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(o[c][i]));  // no use before the wait
+      if (tq >= T) return;
       const float inv = 1.0f / __uint_as_float(o[4][8]);  // column 72: the row sum
+      const size_t row = size_t(I.b) * size_t(T) + size_t(tq);
 #pragma unroll
       for (int g = 0; g < kGroups; ++g) {  // output columns 8 g .. 8 g + 7
         const uint32_t* v = &o[g >> 1][8 * (g & 1)];
@@ -416,8 +443,8 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
             mul_x2(a, b, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), inv, inv);
             hw[i] = __floats2half2_rn(a, b);
           }
-          *reinterpret_cast<uint4*>(stg + 16 * g) = wv;
-        } else if (tq < T) {
+          *reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + row * D + I.h * kDh + 8 * g) = wv;
+        } else {
           uint2 wv;
           __nv_fp8x2_storage_t* q = reinterpret_cast<__nv_fp8x2_storage_t*>(&wv);
 #pragma unroll
@@ -425,37 +452,33 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
             q[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * __uint_as_float(v[2 * i]) * inv,
                                                         16.0f * __uint_as_float(v[2 * i + 1]) * inv),
                                             __NV_SATFINITE, __NV_E4M3);
-          *reinterpret_cast<uint2*>(dst8 + 8 * g) = wv;
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * D + I.h * kDh + 8 * g) = wv;
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(kBarOEmpty + w));  // the next item's first P V may overwrite O
-      if (!p.out_e4m3) {
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && tq0 < T) {
-          tma_store_3d(&tm_out, smem_u32(pbuf + sub * (32 * kDh * 2)), I.h * kDh, tq0, I.b);
-          bulk_commit();
-        }
-      }
-      return true;
     };
+    bool ok = true;
+    if (total > 0) {  // the first item's Q
+      ok = stage_q(0);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kBarQtFull + w));
+    }
     // Reference maximum (log2 units) of this row's P tiles and of the O accumulator
     // in TMEM; the softmax denominator accumulates in O's column 72.
     float m = -INFINITY;
-    bool ok = true;
-    bool pend = false;  // the previous item's output rows were staged at the end of its last tile
-    int staged = 0;     // items whose output went through the staging rows
-
     for (int t = 0; t < total && ok; ++t) {
       const int n = t / nkv, j = t - n * nkv;
-      if (j == 0) m = -INFINITY;
+      // S(t) has finished, and with it every P V product of the group before it
       if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + w), t & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // the whole S row in registers (four loads in flight), then S is released
+      if (j == 0) {
+        if (n > 0) write_item(n - 1);  // O of the previous item is final
+        m = -INFINITY;
+      }
+      // the whole S row in registers (four loads in flight)
       uint32_t sv[4][32];
       tmem_ld32(s_tm, sv[0]);
       tmem_ld32(s_tm + 32, sv[1]);
@@ -465,20 +488,6 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
       reg_fence(sv[1]);
       reg_fence(sv[2]);
       reg_fence(sv[3]);
-      tc_fence_before();
-      mbar_arrive(bar(kBarSEmpty + w));
-      // The previous item's staged output: its store must read the staging rows before
-      // this tile's P overwrites them.
-      bool wait_stage = false;
-      if (pend) {
-        pend = false;
-        if (!p.out_e4m3) {
-          wait_stage = true;
-          if (lane == 0) bulk_wait_read<0>();  // this warp's store has read its staging rows
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarStage + w));
-        }
-      }
       const int valid = T - j * kTile;  // keys of this tile that exist (>= 1)
       if (valid < kTile) {              // keys past the last token: -inf, so P = 0 exactly
 #pragma unroll
@@ -490,23 +499,21 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
       // row maximum: eight independent chains, then combined
       float mq[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mq[k] = fmaxf(__uint_as_float(sv[k >> 1][(k & 1) * 16]), __uint_as_float(sv[k >> 1][(k & 1) * 16 + 1]));
+      for (int k = 0; k < 8; ++k)
+        mq[k] = fmaxf(__uint_as_float(sv[k >> 1][(k & 1) * 16]), __uint_as_float(sv[k >> 1][(k & 1) * 16 + 1]));
 #pragma unroll
       for (int k = 0; k < 8; ++k)
 #pragma unroll
         for (int i = 2; i < 16; i += 2)
-          mq[k] = fmax3(mq[k], __uint_as_float(sv[k >> 1][(k & 1) * 16 + i]), __uint_as_float(sv[k >> 1][(k & 1) * 16 + i + 1]));
+          mq[k] = fmax3(mq[k], __uint_as_float(sv[k >> 1][(k & 1) * 16 + i]),
+                        __uint_as_float(sv[k >> 1][(k & 1) * 16 + i + 1]));
       const float mx = fmaxf(fmaxf(fmax3(mq[0], mq[1], mq[2]), fmax3(mq[3], mq[4], mq[5])), fmaxf(mq[6], mq[7]));
       const float m_tile = mx * sl2;
       const bool raise = m_tile > m + kSlack;  // always on an item's first tile
       const float m_new = raise ? m_tile : m;
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
-        // O (and its row sum) *= 2^(m - m_new), 1 for kept rows, once O += P(t-1) V has finished
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + w), (t - 1) & 1, abort_flag, p.err))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        // O (and its row sum) *= 2^(m - m_new), 1 for kept rows; O holds P V up to
+        // tile t - 1, which finished before S(t) did
         const float f = ex2(m - m_new);
 #pragma unroll 1
         for (int c = 0; c < 10; ++c) {  // 80 columns, 8 at a time (few live registers)
@@ -524,56 +531,39 @@ __global__ void __maxnreg__(168) attention_kernel(const __grid_constant__ CUtens
           }
           tmem_st8(o_tm + 8 * c, e);
         }
-        tmem_st_wait();
       }
       m = m_new;
-      // every warp of the group has finished reading the staging rows (they alias P)
-      if (wait_stage && !__all_sync(0xffffffffu, mbar_wait(bar(kBarStage + w), staged & 1, abort_flag, p.err))) {
+      // P = 2^(scale log2(e) s - m) as F16 pairs (key 2 i in the lower half of column i)
+      // over the first 64 columns of S
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t* s2 = &sv[2 * c + (i >> 4)][2 * (i & 15)];
+          float x0, x1;  // scale log2(e) s - m for two keys in one two-lane FMA
+          fma_x2(x0, x1, __uint_as_float(s2[0]), __uint_as_float(s2[1]), sl2, sl2, -m, -m);
+          const __half2 h = __floats2half2_rn(ex2(x0), ex2(x1));
+          pk[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        tmem_st32(s_tm + 32 * c, pk);
+      }
+      // the item's last S product has finished: the next item's Q may replace Q_w
+      if (j == nkv - 1 && n + 1 < n_my && !stage_q(n + 1)) {
         ok = false;
         break;
       }
-      staged += wait_stage ? 1 : 0;
-      // P = 2^(scale log2(e) s - m) as F16, in two halves of 64 keys; a half's buffer
-      // is free once O += P V of the same half of the previous tile has finished
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarPEmpty + 2 * w + half), (t & 1) ^ 1, abort_flag, p.err))) {
-          ok = false;
-          break;
-        }
-        uint8_t* ph = pbuf + half * (kPBytes / 2);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4 wv;
-            __half2* hw = reinterpret_cast<__half2*>(&wv);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float x0, x1;  // scale log2(e) s - m for two keys in one two-lane FMA
-              fma_x2(x0, x1, __uint_as_float(sv[2 * half + cc][8 * g + 2 * i]),
-                     __uint_as_float(sv[2 * half + cc][8 * g + 2 * i + 1]), sl2, sl2, -m, -m);
-              hw[i] = __floats2half2_rn(ex2(x0), ex2(x1));
-            }
-            *reinterpret_cast<uint4*>(ph + (4 * cc + g) * kGroupBytes + r * 16) = wv;
-          }
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();  // P (generic-proxy stores) visible to the tensor core
-        mbar_arrive(bar(kBarPFull + 2 * w + half));
-      }
-      if (!ok) break;
-
-      if (j == nkv - 1) {  // the item's output rows, once its last P V has finished
-        if (!finish_item(n, t)) {
-          ok = false;
-          break;
-        }
-        pend = true;
-      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPFull + w));
     }
-    if (lane == 0) bulk_wait_all();  // output stores have read shared memory before the CTA exits
+    // the last item's output rows, once the final P V has finished
+    if (ok && total > 0 && __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + w), total & 1, abort_flag, p.err))) {
+      tc_fence_after();
+      write_item(n_my - 1);
+    }
     tmem_ld_wait();
+    tmem_st_wait();
   }
   __syncthreads();
   if (warp == 1) {
@@ -617,21 +607,24 @@ __global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restric
   *reinterpret_cast<uint4*>(dst + cg * kGroupBytes) = u;
 }
 
-// Buffer configuration launched: one Q buffer (both tiles of an item) and 3 + 3 K / V
-// stages. Two Q buffers with 2 + 2 stages, or one with 4 K + 2 V stages, fill the same
-// shared memory and measured slower at 16 heads x 729 tokens (B = 32: 137 us against
-// 139 and 139 us).
+// Buffer configuration launched: one Q staging buffer (both tiles of an item; the
+// next item's queries arrive in it during the current item) and 3 + 3 K / V stages.
 template <int QB, int KS, int VS, bool QK8>
-sv_status attention_launch_cfg(const CUtensorMap& tmo, const Params& p, int grid, cudaStream_t s) {
-  static bool attr_set = false;
+sv_status attention_launch_cfg(const Params& p, int grid, cudaStream_t s) {
   using L = Smem<QB, KS, VS, QK8>;
   auto kern = attention_kernel<QB, KS, VS, QK8>;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  // the attribute is per device: set it once on each device the kernel runs on
+  static unsigned long long attr_set = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice(attention)");
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (!(attr_set & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
-    attr_set = true;
+    attr_set |= bit;
   }
-  cudaError_t e = launch_pdl(kern, dim3(unsigned(grid)), dim3(kThreads), L::kBytes, s, tmo, p);
+  e = launch_pdl(kern, dim3(unsigned(grid)), dim3(kThreads), L::kBytes, s, p);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return SV_OK;
 }
@@ -665,19 +658,8 @@ sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, fl
   const int items = ((T + 2 * kTile - 1) / (2 * kTile)) * H * B;
   const int sms = num_sms() > 0 ? num_sms() : 1;
   const int grid = items < sms ? items : sms;
-  // F16 output rows are written by TMA stores of 32 x 72 blocks: [B][T][D] as a 3-D
-  // tensor, so a block's rows past an image's last token are clipped.
-  CUtensorMap tmo;
-  memset(&tmo, 0, sizeof(tmo));
-  if (!out_e4m3) {
-    const uint64_t dims[3] = {uint64_t(H) * kDh, uint64_t(T), uint64_t(B)};
-    const uint64_t strides[2] = {uint64_t(H) * kDh * 2, uint64_t(T) * H * kDh * 2};
-    const uint32_t box[3] = {uint32_t(kDh), 32, 1};
-    sv_status st = make_tmap(&tmo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, o, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (st != SV_OK) return st;
-  }
-  if (qk8) return attention_launch_cfg<1, 3, 3, true>(tmo, p, grid, s);
-  return attention_launch_cfg<1, 3, 3, false>(tmo, p, grid, s);
+  if (qk8) return attention_launch_cfg<1, 3, 3, true>(p, grid, s);
+  return attention_launch_cfg<1, 3, 3, false>(p, grid, s);
 }
 
 }  // namespace sv
