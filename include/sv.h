@@ -85,6 +85,40 @@ sv_status sv_init_weights_dims(uint64_t seed, int tokens, int patch_dim, int wid
 /* Model dimensions of the resident weights (any pointer may be NULL). */
 sv_status sv_model_dims(int* tokens, int* patch_dim, int* width, int* heads, int* mlp, int* layers);
 
+/*
+ * Number of parameter values of the resident model (0 before sv_init_*): the
+ * sum over its tensors of rows x cols, in the tensor order of synth/synth.h.
+ */
+size_t sv_weights_count(void);
+
+/*
+ * Copies the resident parameters back to the host: every tensor in the order
+ * of synth/synth.h, each in its logical row-major layout ([fan_in, fan_out] for
+ * a dense weight, i.e. the transpose of the [N, K] copy the GEMMs read; the K
+ * padding of the patch weight is left out), each F16 value widened to F32
+ * exactly. This is what the pages' resident loop saves as its reference
+ * weights ("FP8 attention and resident image/embedding transfers", Resident
+ * inference loop). The QKV and MLP-up weights are resident with their
+ * LayerNorm scale folded in (gamma_k W[k][n], rounded to F16 once), which is W
+ * itself for the scale-1 initialisation.
+ * host_dst: caller-owned host memory of at least n_floats = sv_weights_count()
+ * values. Synchronous. Errors: SV_ERR_NOT_INITIALIZED; SV_ERR_INVALID_ARG if
+ * host_dst is NULL or n_floats is too small; SV_ERR_CUDA.
+ */
+sv_status sv_export_weights(float* host_dst, size_t n_floats);
+
+/* Number of bytes sv_export_weights_e4m3 writes (0 before sv_init_*). */
+size_t sv_weights_count_e4m3(void);
+
+/*
+ * Copies the E4M3 copies of the resident weights back to the host: the dense
+ * weights and the MAP probe (the tensors an E4M3 GEMM reads), in the order of
+ * synth/synth.h, each in its logical row-major layout as in sv_export_weights,
+ * one E4M3 code of 16 w per byte. host_dst: at least sv_weights_count_e4m3()
+ * bytes. Synchronous. Errors: as sv_export_weights.
+ */
+sv_status sv_export_weights_e4m3(uint8_t* host_dst, size_t n_bytes);
+
 /* ---------------------------------------------------------------- forward */
 
 /*
@@ -173,8 +207,9 @@ sv_status sv_pack_patches(const void* images, void* pixels, int batch, int image
  * A dense projection with its fused epilogue ("SigLIP ViT benchmark":
  * projections with bias, GELU, residual adds). W is stored [N, K] (K-major,
  * i.e. the transpose of the logical [fan_in, fan_out] weight).
- *   in_dtype SV_GEMM_F16: A, W f16; SV_GEMM_E4M3: A, W e4m3 codes and the
- *     caller passes scale = 2^-8 to undo the two 2^4 operand scales.
+ *   scale = scale_a * scale_w, the dequantisation scales of the two operands.
+ *   in_dtype SV_GEMM_F16: A, W f16 (scales 1); SV_GEMM_E4M3: A, W e4m3 codes of
+ *     16 a and 16 w, so the caller passes scale_a = scale_w = 2^-4.
  *   bias: f16 [N] or NULL. pos: f16 [pos_rows, N] or NULL (added by row
  *     m % pos_rows: the positional embedding of the patch-embedding GEMM).
  *   residual: f16 [M, N] or NULL; it may alias C (each element is read
@@ -187,16 +222,23 @@ sv_status sv_pack_patches(const void* images, void* pixels, int batch, int image
  */
 sv_status sv_gemm_bias_act(const void* A, const void* W, const void* bias, const void* pos, int pos_rows,
                            const void* residual, void* C, int M, int N, int K, int act, int in_dtype, int out_dtype,
-                           float scale, void* stream);
+                           float scale_a, float scale_w, void* stream);
 
 /*
  * y = (x - mean) / sqrt(var + eps) * gamma + beta per row, mean and biased
- * centred variance in F32 ("SigLIP ViT benchmark", LayerNorm paragraph).
- * x: f16 [rows, width]; gamma, beta: f16 [width]; y: [rows, width] f16 or
- * e4m3 (out_dtype). Requirements: width % 8 == 0, 8 <= width <= 4096.
+ * centred variance in F32 ("SigLIP ViT benchmark", LayerNorm paragraph), with an
+ * optional residual add in front ("SigLIP ViT benchmark", LayerNorm/Add
+ * paragraph: the residual adds of the encoder; "Performance follow-up": LN and
+ * Add as the follow-up targets).
+ * x: f16 [rows, width]. residual: f16 [rows, width] or NULL; when given, each
+ *   row is first replaced by x + residual (added in F32, rounded to F16 once),
+ *   which is written back to x, and y is the LayerNorm of that F16 sum.
+ * gamma, beta: f16 [width]; y: [rows, width] f16 or e4m3 (out_dtype); y must
+ * not overlap x or residual. Requirements: width % 8 == 0, 8 <= width <= 4096;
+ * pointers 16-byte aligned.
  */
-sv_status sv_layernorm(const void* x, const void* gamma, const void* beta, void* y, int rows, int width, float eps,
-                       int out_dtype, void* stream);
+sv_status sv_layernorm(void* x, const void* residual, const void* gamma, const void* beta, void* y, int rows,
+                       int width, float eps, int out_dtype, void* stream);
 
 /*
  * C[M,N] = act(LayerNorm(x)[M,K] . W[N,K]^T + bias[N]), F16 in and out: a
@@ -225,8 +267,10 @@ sv_status sv_ln_gemm(const void* x, const void* gamma, const void* beta, float e
  *   inside each third ("fused QKV" section: slices with head views).
  * o: [batch, tokens, heads * head_dim] f16 or e4m3 (out_dtype), head h at
  *   columns h*head_dim.. (heads concatenated).
- * o_h = softmax(scale * Q_h K_h^T) V_h. Requirements: head_dim == 72,
- * tokens >= 1, heads >= 1.
+ * o_h = softmax(scale * Q_h K_h^T) V_h; scale <= 0 selects 1 / sqrt(head_dim)
+ * (scaled dot-product attention). Requirements: head_dim == 72, tokens >= 1,
+ * heads >= 1. The call keeps a scratch buffer (the head-blocked copy of qkv) that
+ * grows to the largest call and is freed by sv_shutdown.
  */
 sv_status sv_attention(const void* qkv, void* o, int batch, int heads, int tokens, int head_dim, float scale,
                        int out_dtype, void* stream);
@@ -248,6 +292,17 @@ sv_status sv_attention_ex(const void* qkv, void* o, int batch, int heads, int to
                           int out_dtype, int flags, void* stream);
 
 /*
+ * The same attention with Q, K and V given per head: q, k, v: f16 [batch, heads,
+ * tokens, head_stride], head_stride >= head_dim values per row of which the
+ * first head_dim are used (e.g. 80: the head width 72 padded to the tensor
+ * core's step; the pad values are never read). o, scale, out_dtype and flags as
+ * in sv_attention_ex. Requirements: head_dim == 72, head_stride % 8 == 0,
+ * head_stride <= 4096; pointers 16-byte aligned.
+ */
+sv_status sv_attention_heads(const void* q, const void* k, const void* v, void* o, int batch, int heads, int tokens,
+                             int head_dim, int head_stride, float scale, int out_dtype, int flags, void* stream);
+
+/*
  * MAP pooling head with the resident weights ("SigLIP ViT benchmark":
  * shared learned probe, its own Q projection, the fused KV projection,
  * multi-head cross-attention, output projection, LayerNorm/MLP residual).
@@ -265,14 +320,19 @@ sv_status sv_map_pool(const void* x, void* out, int batch, int gemm_dtype, void*
  * budget. Same arguments, computation and results as sv_map_pool (it uses the
  * resident weights of sv_init_weights, which the caller sets up beforehand);
  * images are pooled one at a time, so it is slower for large batches.
- * Its scratch is one static device array of 8 MiB compiled into the library,
- * held by every GPU that loads the library until the process exits. With the
- * So400m/14 sizes that admits 1..256 images per call; larger batches (or
- * models whose scratch would not fit) are rejected with SV_ERR_INVALID_ARG.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture. All calls share the array: calls whose GPU work overlaps
- * (other streams or threads) race and must be serialised by the caller.
+ * Its scratch is one static device array of 8 MiB compiled into the library.
+ * The array is placed in a device's memory when the library's code is loaded
+ * into that device's context (with CUDA's default lazy loading, at the first
+ * sv_map_pool_static call on the device) and stays there until the context is
+ * destroyed. With the So400m/14 sizes that admits 1..256 images per call;
+ * larger batches (or models whose scratch would not fit) are rejected with
+ * SV_ERR_INVALID_ARG. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current and keeps it; make
+ * that first call before any stream capture. sv_shutdown forgets the kept
+ * addresses: a caller that resets or destroys a device's context must call
+ * sv_shutdown before doing so. All calls share the array, and it keeps the
+ * previous call's contents: calls whose GPU work overlaps (other streams or
+ * threads) race on it and must be serialised by the caller.
  */
 sv_status sv_map_pool_static(const void* x, void* out, int batch, int gemm_dtype, void* stream);
 
@@ -327,6 +387,32 @@ sv_status sv_debug_fill_workspace(int batch, int gemm_dtype, int byte_value);
  * the context stays usable. Exercises the bounded-wait path every kernel uses.
  */
 sv_status sv_debug_wait_timeout(unsigned int limit_us, void* stream);
+
+/* Stages of the forward pass that sv_debug_encode_stage can stop after. */
+typedef enum {
+  SV_STAGE_PATCH = 0,     /* X after the patch embedding: f16 [batch*tokens, width] */
+  SV_STAGE_QKV = 1,       /* [Q | K | V] of the last layer, row-major f16 [batch*tokens, 3*width] */
+  SV_STAGE_ATTENTION = 2, /* attention output O of the last layer: [batch*tokens, width] */
+  SV_STAGE_OUT_PROJ = 3,  /* X after the output projection + residual of the last layer (f16) */
+  SV_STAGE_MLP_UP = 4,    /* GELU output of the last layer's MLP: [batch*tokens, mlp] */
+  SV_STAGE_MLP_DOWN = 5,  /* X after the last layer (f16) */
+  SV_STAGE_FINAL_LN = 6   /* output of the final LayerNorm: [batch*tokens, width] */
+} sv_stage;
+
+/*
+ * Test hook for per-stage parity: runs sv_encode_ex's launches one by one for
+ * `batch` images through `layers` layers, stops after `stage` (of the last
+ * layer), and copies that stage's output tensor into dst (caller-owned device
+ * memory of at least dst_bytes; the sizes and types are in sv_stage: f16, or for
+ * O, the MLP hidden and the final LayerNorm with gemm_dtype SV_GEMM_E4M3 the
+ * e4m3 codes the next GEMM reads). SV_STAGE_QKV with SV_ENCODE_FP8_ATTENTION
+ * (E4M3 Q and K) is not supported. Uses the cached workspace of
+ * (batch, gemm_dtype, flags) and the caller's stream; the output buffer of
+ * sv_encode is not written.
+ * Errors: as sv_encode_ex; SV_ERR_INVALID_ARG if dst_bytes is too small.
+ */
+sv_status sv_debug_encode_stage(const void* pixels, int batch, int layers, int gemm_dtype, int flags, int stage,
+                                void* dst, size_t dst_bytes, void* stream);
 
 /* Frees the weights, workspaces and events; the library can be re-initialised. */
 void sv_shutdown(void);

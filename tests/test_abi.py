@@ -66,15 +66,15 @@ def test_errors_before_device_work(lib):
     buf = (ctypes.c_uint8 * 4096)()
     p16 = (ctypes.addressof(buf) + 15) // 16 * 16
     # N not a multiple of 16
-    assert lib.sv_gemm_bias_act(p16, p16, None, None, 1, None, p16, 16, 15, 16, 0, 0, 0, 1.0, None) == \
+    assert lib.sv_gemm_bias_act(p16, p16, None, None, 1, None, p16, 16, 15, 16, 0, 0, 0, 1.0, 1.0, None) == \
         vt.SV_ERR_INVALID_ARG
     # misaligned operand
-    assert lib.sv_gemm_bias_act(p16 + 2, p16, None, None, 1, None, p16, 16, 16, 16, 0, 0, 0, 1.0, None) == \
+    assert lib.sv_gemm_bias_act(p16 + 2, p16, None, None, 1, None, p16, 16, 16, 16, 0, 0, 0, 1.0, 1.0, None) == \
         vt.SV_ERR_INVALID_ARG
     # bad activation / dtype codes
-    assert lib.sv_gemm_bias_act(p16, p16, None, None, 1, None, p16, 16, 16, 16, 7, 0, 0, 1.0, None) == \
+    assert lib.sv_gemm_bias_act(p16, p16, None, None, 1, None, p16, 16, 16, 16, 7, 0, 0, 1.0, 1.0, None) == \
         vt.SV_ERR_INVALID_ARG
-    assert lib.sv_gemm_bias_act(p16, p16, None, None, 1, None, p16, 16, 16, 16, 0, 3, 0, 1.0, None) == \
+    assert lib.sv_gemm_bias_act(p16, p16, None, None, 1, None, p16, 16, 16, 16, 0, 3, 0, 1.0, 1.0, None) == \
         vt.SV_ERR_INVALID_ARG
     # image packing: side not a multiple of the patch
     assert lib.sv_pack_patches(p16, p16, 1, 30, 3, 14, None) == vt.SV_ERR_INVALID_ARG
@@ -82,10 +82,16 @@ def test_errors_before_device_work(lib):
     assert lib.sv_ln_gemm(p16, p16, p16, 1e-6, p16, None, p16, 16, 16, 8192, 0, None) == vt.SV_ERR_INVALID_ARG
     assert lib.sv_ln_gemm(p16, p16, p16, 1e-6, p16, None, p16, 16, 24, 16, 0, None) == vt.SV_ERR_INVALID_ARG
     # LayerNorm width must be a multiple of 8 (even, unpadded rows: LayerNorm paragraph)
-    assert lib.sv_layernorm(p16, p16, p16, p16, 4, 12, 1e-6, 0, None) == vt.SV_ERR_INVALID_ARG
+    assert lib.sv_layernorm(p16, None, p16, p16, p16, 4, 12, 1e-6, 0, None) == vt.SV_ERR_INVALID_ARG
+    # ... and its residual operand 16-byte aligned
+    assert lib.sv_layernorm(p16, p16 + 2, p16, p16, p16, 4, 16, 1e-6, 0, None) == vt.SV_ERR_INVALID_ARG
     # head width other than 72 is not implemented
     assert lib.sv_attention(p16, p16, 1, 2, 4, 64, 0.125, 0, None) == vt.SV_ERR_UNSUPPORTED
     assert lib.sv_attention(p16, p16, 0, 2, 4, 72, 0.125, 0, None) == vt.SV_ERR_INVALID_ARG
+    # per-head operands: the row stride must cover the head and keep 16-byte rows
+    assert lib.sv_attention_heads(p16, p16, p16, p16, 1, 2, 4, 72, 64, 0.0, 0, 0, None) == vt.SV_ERR_INVALID_ARG
+    assert lib.sv_attention_heads(p16, p16, p16, p16, 1, 2, 4, 72, 76, 0.0, 0, 0, None) == vt.SV_ERR_INVALID_ARG
+    assert lib.sv_attention_heads(p16, p16, p16, p16, 1, 2, 4, 64, 80, 0.0, 0, 0, None) == vt.SV_ERR_UNSUPPORTED
     # unknown attention option bits
     assert lib.sv_attention_ex(p16, p16, 1, 2, 4, 72, 0.125, 0, 2, None) == vt.SV_ERR_INVALID_ARG
     # quantiser length
@@ -98,4 +104,8 @@ def test_errors_before_device_work(lib):
     # nothing initialised yet
     assert lib.sv_encode(p16, p16, 1, 1, 0, None) == vt.SV_ERR_NOT_INITIALIZED
     assert lib.sv_map_pool(p16, p16, 1, 0, None) == vt.SV_ERR_NOT_INITIALIZED
+    assert lib.sv_weights_count() == 0 and lib.sv_weights_count_e4m3() == 0
+    assert lib.sv_export_weights(p16, 16) == vt.SV_ERR_NOT_INITIALIZED
+    assert lib.sv_export_weights_e4m3(p16, 16) == vt.SV_ERR_NOT_INITIALIZED
+    assert lib.sv_debug_encode_stage(p16, 1, 1, 0, 0, 0, p16, 16, None) == vt.SV_ERR_NOT_INITIALIZED
     assert b"sv_init_weights" in lib.sv_last_error()

@@ -56,6 +56,24 @@ def test_gemm_f16_bias(sv, M, N, K):
     assert_close(host(C), ref, RT, RT * _scale(ref), f"gemm {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K,act,res", [
+    (5832, 4304, 1152, 1, False),  # MLP up + GELU at batch 8
+    (5832, 1152, 4304, 0, True),   # MLP down + residual at batch 8
+    (5832, 1152, 1152, 0, True),   # output projection + residual at batch 8
+])
+def test_gemm_batch8_mlp_shapes(sv, M, N, K, act, res):
+    """The encoder's MLP and output-projection GEMMs at the single-layer batch-8
+    configuration's size (5832 = 8 x 729 rows), element by element."""
+    A, W, b = _gemm_inputs(25, M, N, K)
+    R = synth.normal(25, 4, (M, N)) if res else None
+    C = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    sv.sv_gemm_bias_act(dev_f16(A), dev_f16(W.T), dev_f16(b), None, 1, dev_f16(R) if res else None, C, M, N, K,
+                        act=act)
+    sv.sv_sync()
+    ref = oracle.linear(A, W, b, residual=R, act=act)
+    assert_close(host(C), ref, RT, RT * _scale(ref), f"gemm {M}x{N}x{K} act {act} residual {res}")
+
+
 def test_gemm_epilogues_gelu_residual_pos(sv):
     M, N, K = 777, 4304, 1152
     A, W, b = _gemm_inputs(31, M, N, K)
@@ -101,7 +119,7 @@ def test_gemm_e4m3(sv, M, N, K):
     sv.sv_quantize_e4m3(dev_f16(A), A8, M * K)
     sv.sv_quantize_e4m3(dev_f16(W.T), W8, N * K)
     C = torch.empty(M, N, dtype=torch.float16, device="cuda")
-    sv.sv_gemm_bias_act(A8, W8, dev_f16(b), None, 1, None, C, M, N, K, in_dtype=1, scale=2.0 ** -8)
+    sv.sv_gemm_bias_act(A8, W8, dev_f16(b), None, 1, None, C, M, N, K, in_dtype=1, scale_a=2.0 ** -4, scale_w=2.0 ** -4)
     sv.sv_sync()
     ref = oracle.linear(A, W, b, fp8=True)
     assert_close(host(C), ref, RT, RT * _scale(ref), f"e4m3 gemm {M}x{N}x{K}")
@@ -127,14 +145,40 @@ def test_layernorm(sv, rows, width):
     g = synth.normal(70, 2, (width,), mean=1.0, std=0.2)
     bt = synth.normal(70, 3, (width,), std=0.2)
     y = torch.empty(rows, width, dtype=torch.float16, device="cuda")
-    sv.sv_layernorm(dev_f16(x), dev_f16(g), dev_f16(bt), y, rows, width)
+    sv.sv_layernorm(dev_f16(x), None, dev_f16(g), dev_f16(bt), y, rows, width)
     sv.sv_sync()
     ref = oracle.layernorm(x, g, bt)
     assert_close(host(y), ref, RT, RT, f"layernorm {rows}x{width}")
     y8 = torch.empty(rows, width, dtype=torch.uint8, device="cuda")
-    sv.sv_layernorm(dev_f16(x), dev_f16(g), dev_f16(bt), y8, rows, width, out_dtype=1)
+    sv.sv_layernorm(dev_f16(x), None, dev_f16(g), dev_f16(bt), y8, rows, width, out_dtype=1)
     sv.sv_sync()
     assert_close(decode_e4m3(y8).reshape(rows, width), ref, 2.0 ** -3 + RT, 2.0 ** -10, "layernorm e4m3")
+
+
+@pytest.mark.parametrize("rows,width", [(1, 1152), (37, 144), (5832, 1152), (1000, 4096)])
+def test_layernorm_residual(sv, rows, width):
+    """y = LN(x + res) with the F16 sum written back to x ("SigLIP ViT benchmark",
+    LayerNorm/Add paragraph). The sum is one F32 add of two F16 values rounded to
+    F16, so the written-back x is bit-exact against the same rounding in numpy; y is
+    checked against the oracle's LayerNorm of that sum at the LayerNorm tolerance."""
+    x = (synth.normal(72, 1, (rows, width)).astype(np.float32) * 3 + 1.5).astype(np.float16)
+    r = synth.normal(72, 4, (rows, width), std=2.0)
+    g = synth.normal(72, 2, (width,), mean=1.0, std=0.2)
+    bt = synth.normal(72, 3, (width,), std=0.2)
+    xs = (x.astype(np.float32) + r.astype(np.float32)).astype(np.float16)
+    xd = dev_f16(x)
+    y = torch.empty(rows, width, dtype=torch.float16, device="cuda")
+    sv.sv_layernorm(xd, dev_f16(r), dev_f16(g), dev_f16(bt), y, rows, width)
+    sv.sv_sync()
+    assert np.array_equal(xd.cpu().numpy().view(np.uint16), xs.view(np.uint16))
+    ref = oracle.layernorm(xs, g, bt)
+    assert_close(host(y), ref, RT, RT, f"layernorm+residual {rows}x{width}")
+    # E4M3 output from the same sum (x now holds it; a zero residual leaves it unchanged)
+    y8 = torch.empty(rows, width, dtype=torch.uint8, device="cuda")
+    sv.sv_layernorm(xd, dev_f16(np.zeros_like(r)), dev_f16(g), dev_f16(bt), y8, rows, width, out_dtype=1)
+    sv.sv_sync()
+    assert np.array_equal(xd.cpu().numpy(), xs)
+    assert_close(decode_e4m3(y8).reshape(rows, width), ref, 2.0 ** -3 + RT, 2.0 ** -10, "layernorm+residual e4m3")
 
 
 @pytest.mark.parametrize("M,N,K,act", [(729, 3456, 1152, 0), (777, 4304, 1152, 1), (200, 48, 80, 0)])
@@ -191,6 +235,31 @@ def test_attention(sv, B, H, T, sharp):
     ref = _attn_ref(qkv, H)
     vmax = float(np.abs(qkv[..., 2 * D:].astype(np.float64)).max())
     assert_close(host(o), ref, RT, RT * vmax, f"attention B{B} H{H} T{T}")
+
+
+@pytest.mark.parametrize("B,H,T,stride", [(2, 16, 729, 80), (1, 3, 200, 72), (3, 4, 300, 96), (1, 2, 1, 80)])
+def test_attention_heads(sv, B, H, T, stride):
+    """Per-head Q, K, V [B, H, T, stride]: the columns past the head width are NaN and
+    never read; the result equals the attention of the same values in the fused
+    layout, and the default scale (0 -> 1/sqrt(72)) equals the explicit one."""
+    D = H * 72
+    qkv = synth.normal(280 + T, 1, (B, T, 3 * D))
+    heads = []
+    for j in range(3):
+        a = np.full((B, H, T, stride), np.nan, dtype=np.float16)
+        a[..., :72] = qkv[..., j * D:(j + 1) * D].reshape(B, T, H, 72).transpose(0, 2, 1, 3)
+        heads.append(dev_f16(a))
+    o = torch.full((B, T, D), float("nan"), dtype=torch.float16, device="cuda")
+    sv.sv_attention_heads(heads[0], heads[1], heads[2], o, B, H, T, head_stride=stride)
+    sv.sv_sync()
+    ref = _attn_ref(qkv, H)
+    vmax = float(np.abs(qkv[..., 2 * D:].astype(np.float64)).max())
+    assert_close(host(o), ref, RT, RT * vmax, f"attention (per head) B{B} H{H} T{T} stride {stride}")
+    o2 = torch.empty_like(o)
+    s32 = float(np.float32(1.0) / np.sqrt(np.float32(72.0)))  # 1/sqrt(72) rounded as the library's F32 does
+    sv.sv_attention_heads(heads[0], heads[1], heads[2], o2, B, H, T, head_stride=stride, scale=s32)
+    sv.sv_sync()
+    assert torch.equal(o, o2)
 
 
 @pytest.mark.parametrize("B,H,T,sharp", [(1, 2, 4, 1.0), (2, 16, 729, 1.0), (1, 3, 200, 3.0), (3, 4, 300, 1.5),

@@ -31,14 +31,19 @@ SIGNATURES = [
     ("sv_init_weights", _I, [_U64]),
     ("sv_init_weights_dims", _I, [_U64, _I, _I, _I, _I, _I, _I]),
     ("sv_model_dims", _I, [_IP, _IP, _IP, _IP, _IP, _IP]),
+    ("sv_weights_count", _SZ, []),
+    ("sv_export_weights", _I, [_VP, _SZ]),
+    ("sv_weights_count_e4m3", _SZ, []),
+    ("sv_export_weights_e4m3", _I, [_VP, _SZ]),
     ("sv_encode", _I, [_VP, _VP, _I, _I, _I, _VP]),
     ("sv_encode_ex", _I, [_VP, _VP, _I, _I, _I, _I, _VP]),
-    ("sv_gemm_bias_act", _I, [_VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
-    ("sv_layernorm", _I, [_VP, _VP, _VP, _VP, _I, _I, _F, _I, _VP]),
+    ("sv_gemm_bias_act", _I, [_VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _F, _VP]),
+    ("sv_layernorm", _I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _F, _I, _VP]),
     ("sv_ln_gemm", _I, [_VP, _VP, _VP, _F, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     ("sv_pack_patches", _I, [_VP, _VP, _I, _I, _I, _I, _VP]),
     ("sv_attention", _I, [_VP, _VP, _I, _I, _I, _I, _F, _I, _VP]),
     ("sv_attention_ex", _I, [_VP, _VP, _I, _I, _I, _I, _F, _I, _I, _VP]),
+    ("sv_attention_heads", _I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _VP]),
     ("sv_map_pool", _I, [_VP, _VP, _I, _I, _VP]),
     ("sv_map_pool_static", _I, [_VP, _VP, _I, _I, _VP]),
     ("sv_quantize_e4m3", _I, [_VP, _VP, _SZ, _VP]),
@@ -50,6 +55,7 @@ SIGNATURES = [
     ("sv_profile_read", _I, [_I, _DP, _DP, _DP, _LLP]),
     ("sv_debug_fill_workspace", _I, [_I, _I, _I]),
     ("sv_debug_wait_timeout", _I, [ctypes.c_uint, _VP]),
+    ("sv_debug_encode_stage", _I, [_VP, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
     ("sv_shutdown", None, []),
 ]
 
@@ -92,6 +98,13 @@ def _ptr(x):
     return x.data_ptr()
 
 
+def _hptr(x):
+    """Host buffer address: an int, or an object with a numpy-style ctypes.data."""
+    if isinstance(x, int):
+        return x
+    return x.ctypes.data
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -119,6 +132,8 @@ SV_ENCODE_UNFUSED_QKV = 1
 SV_ENCODE_FP8_ATTENTION = 2
 SV_ENCODE_EAGER = 4
 SV_ATTENTION_QK_E4M3 = 1
+(SV_STAGE_PATCH, SV_STAGE_QKV, SV_STAGE_ATTENTION, SV_STAGE_OUT_PROJ, SV_STAGE_MLP_UP, SV_STAGE_MLP_DOWN,
+ SV_STAGE_FINAL_LN) = range(7)
 
 
 def sv_encode_ex(pixels, out, batch: int, layers: int, gemm_dtype: int = SV_GEMM_F16, flags: int = 0, stream=None):
@@ -131,10 +146,10 @@ def sv_encode(pixels, out, batch: int, layers: int, gemm_dtype: int = SV_GEMM_F1
 
 
 def sv_gemm_bias_act(A, W, bias, pos, pos_rows: int, residual, C, M: int, N: int, K: int, act: int = 0,
-                     in_dtype: int = 0, out_dtype: int = 0, scale: float = 1.0, stream=None):
+                     in_dtype: int = 0, out_dtype: int = 0, scale_a: float = 1.0, scale_w: float = 1.0, stream=None):
     _check("sv_gemm_bias_act", load().sv_gemm_bias_act(_ptr(A), _ptr(W), _ptr(bias), _ptr(pos), pos_rows,
                                                        _ptr(residual), _ptr(C), M, N, K, act, in_dtype, out_dtype,
-                                                       scale, _stream(stream)))
+                                                       scale_a, scale_w, _stream(stream)))
 
 
 def sv_pack_patches(images, pixels, batch: int, image_side: int = 378, channels: int = 3, patch: int = 14,
@@ -148,23 +163,47 @@ def sv_ln_gemm(x, gamma, beta, W, bias, C, M: int, N: int, K: int, act: int = 0,
                                            K, act, _stream(stream)))
 
 
-def sv_layernorm(x, gamma, beta, y, rows: int, width: int, eps: float = 1e-6, out_dtype: int = 0, stream=None):
-    _check("sv_layernorm", load().sv_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), rows, width, eps,
-                                               out_dtype, _stream(stream)))
+def sv_layernorm(x, residual, gamma, beta, y, rows: int, width: int, eps: float = 1e-6, out_dtype: int = 0,
+                 stream=None):
+    _check("sv_layernorm", load().sv_layernorm(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(beta), _ptr(y), rows,
+                                               width, eps, out_dtype, _stream(stream)))
 
 
-def sv_attention(qkv, o, batch: int, heads: int, tokens: int, head_dim: int = 72, scale: float | None = None,
+def sv_attention(qkv, o, batch: int, heads: int, tokens: int, head_dim: int = 72, scale: float = 0.0,
                  out_dtype: int = 0, stream=None):
-    s = head_dim ** -0.5 if scale is None else scale
-    _check("sv_attention", load().sv_attention(_ptr(qkv), _ptr(o), batch, heads, tokens, head_dim, s, out_dtype,
+    """scale <= 0 lets the library use 1/sqrt(head_dim)."""
+    _check("sv_attention", load().sv_attention(_ptr(qkv), _ptr(o), batch, heads, tokens, head_dim, scale, out_dtype,
                                                _stream(stream)))
 
 
-def sv_attention_ex(qkv, o, batch: int, heads: int, tokens: int, head_dim: int = 72, scale: float | None = None,
+def sv_attention_ex(qkv, o, batch: int, heads: int, tokens: int, head_dim: int = 72, scale: float = 0.0,
                     out_dtype: int = 0, flags: int = 0, stream=None):
-    s = head_dim ** -0.5 if scale is None else scale
-    _check("sv_attention_ex", load().sv_attention_ex(_ptr(qkv), _ptr(o), batch, heads, tokens, head_dim, s,
+    _check("sv_attention_ex", load().sv_attention_ex(_ptr(qkv), _ptr(o), batch, heads, tokens, head_dim, scale,
                                                      out_dtype, flags, _stream(stream)))
+
+
+def sv_attention_heads(q, k, v, o, batch: int, heads: int, tokens: int, head_dim: int = 72, head_stride: int = 80,
+                       scale: float = 0.0, out_dtype: int = 0, flags: int = 0, stream=None):
+    _check("sv_attention_heads", load().sv_attention_heads(_ptr(q), _ptr(k), _ptr(v), _ptr(o), batch, heads, tokens,
+                                                           head_dim, head_stride, scale, out_dtype, flags,
+                                                           _stream(stream)))
+
+
+def sv_weights_count() -> int:
+    return int(load().sv_weights_count())
+
+
+def sv_export_weights(host_dst, n_floats: int):
+    """host_dst: a writable float32 buffer (e.g. a numpy array's ctypes data pointer) of n_floats values."""
+    _check("sv_export_weights", load().sv_export_weights(_hptr(host_dst), n_floats))
+
+
+def sv_weights_count_e4m3() -> int:
+    return int(load().sv_weights_count_e4m3())
+
+
+def sv_export_weights_e4m3(host_dst, n_bytes: int):
+    _check("sv_export_weights_e4m3", load().sv_export_weights_e4m3(_hptr(host_dst), n_bytes))
 
 
 def sv_map_pool(x, out, batch: int, gemm_dtype: int = SV_GEMM_F16, stream=None):
@@ -212,6 +251,12 @@ def sv_debug_fill_workspace(batch: int, gemm_dtype: int, byte_value: int):
 
 def sv_debug_wait_timeout(limit_us: int, stream=None):
     _check("sv_debug_wait_timeout", load().sv_debug_wait_timeout(limit_us, _stream(stream)))
+
+
+def sv_debug_encode_stage(pixels, batch: int, layers: int, gemm_dtype: int, flags: int, stage: int, dst,
+                          dst_bytes: int, stream=None):
+    _check("sv_debug_encode_stage", load().sv_debug_encode_stage(_ptr(pixels), batch, layers, gemm_dtype, flags, stage,
+                                                                 _ptr(dst), dst_bytes, _stream(stream)))
 
 
 def sv_shutdown():

@@ -51,23 +51,7 @@ cudaEvent_t get_event() {
   return e;
 }
 
-// Counts one launch and, when profiling is on, brackets it with events.
-struct Launch {
-  bool on;
-  cudaStream_t stream = nullptr;
-  Launch(int kind, double flops, double bytes, cudaStream_t s) : on(g_prof_on) {
-    ++g_launches;
-    if (on) {
-      ProfRec r{kind, flops, bytes, get_event(), get_event()};
-      cudaEventRecord(r.e0, s);
-      g_prof.push_back(r);
-      stream = s;
-    }
-  }
-  ~Launch() {
-    if (on) cudaEventRecord(g_prof.back().e1, stream);
-  }
-};
+using Launch = LaunchScope;
 
 // ------------------------------------------------------------ model state
 struct Dims {
@@ -82,9 +66,20 @@ struct LayerW {
   __half *qkv_aug, *qkv_bf, *fc1_aug, *fc1_bf;
 };
 
+// One parameter tensor as drawn (synth order): its resident F16 copy ([N, kpad]
+// K-major for a dense weight, else row-major) and its E4M3 copy, if any.
+struct TensorRec {
+  int rows = 0, cols = 0;  // logical [rows, cols] (a dense weight: [K, N])
+  bool matrix = false;
+  int kpad = 0;
+  const __half* p16 = nullptr;
+  const uint8_t* p8 = nullptr;
+};
+
 struct Weights {
   bool ready = false;
   Dims d;
+  std::vector<TensorRec> tensors;
   void* arena = nullptr;
   void* fold = nullptr;  // extra K block rows and combined biases of the folded LayerNorms
   __half *patch_w = nullptr, *patch_b = nullptr, *pos = nullptr;
@@ -268,6 +263,14 @@ sv_status init_weights(uint64_t seed, const Dims& d) {
     SV_CHECK_CUDA(cudaMemcpy(p16, host.data(), 2 * elems, cudaMemcpyHostToDevice), "weight upload");
     uint8_t* p8 = s.off8 ? reinterpret_cast<uint8_t*>(base + s.off8) : nullptr;
     if (p8) SV_TRY(quantize_launch(p16, p8, elems, nullptr));
+    TensorRec rec;
+    rec.rows = s.info.rows;
+    rec.cols = s.info.cols;
+    rec.matrix = s.matrix;
+    rec.kpad = s.kpad;
+    rec.p16 = p16;
+    rec.p8 = p8;
+    g_w.tensors.push_back(rec);
     const int l = s.info.layer;
     if (l >= 0) {
       LayerW& w = g_w.layers[size_t(l)];
@@ -553,7 +556,9 @@ sv_status run_map(MapPlan& m, int B, int fp8, __half* out, cudaStream_t s) {
   return run_gemm(m.fc2, s);
 }
 
-sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStream_t s) {
+// The forward pass. stop >= 0 (a test hook, see sv_debug_encode_stage) returns after
+// that sv_stage of the last layer instead of running to the end.
+sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStream_t s, int stop = -1) {
   const Dims& d = g_w.d;
   const int B = p.B, fp8 = p.fp8;
   const int M = B * d.T;
@@ -562,23 +567,31 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
     SV_TRY(pad_pixels_launch(pixels, p.A0, M, d.P, d.Kp, fp8, s));
   }
   SV_TRY(run_gemm(p.patch, s));
+  if (stop == SV_STAGE_PATCH) return SV_OK;
   for (int l = 0; l < layers; ++l) {
     const LayerW& w = g_w.layers[size_t(l)];
     const size_t i = size_t(l);
+    const bool last = l == layers - 1;
     SV_TRY(p.fold_ln ? run_ln_finalize(p, l == 0 ? p.patch : p.fc2[i - 1], M, s)
                      : run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
     for (int j = 0; j < p.qkv_calls; ++j) SV_TRY(run_gemm(p.qkv[i * size_t(p.qkv_calls) + size_t(j)], s));
+    if (last && stop == SV_STAGE_QKV) return SV_OK;
     {
       Launch L(kKindAttn, 4.0 * B * d.H * double(d.T) * double(d.T) * 72.0,
                double(M) * d.D * (2 * (p.qk8 ? 1.0 : 2.0) + 2.0) + double(M) * d.D * (fp8 ? 1.0 : 2.0), s);
       SV_TRY(attention_launch(p.QKV, p.O, B, d.T, d.H, 1.0f / std::sqrt(72.0f), fp8, p.qk8, s));
     }
+    if (last && stop == SV_STAGE_ATTENTION) return SV_OK;
     SV_TRY(run_gemm(p.out[i], s));
+    if (last && stop == SV_STAGE_OUT_PROJ) return SV_OK;
     SV_TRY(p.fold_ln ? run_ln_finalize(p, p.out[i], M, s) : run_ln(p.X, w.ln2_g, w.ln2_b, p.Y, M, fp8, s));
     SV_TRY(run_gemm(p.fc1[i], s));
+    if (last && stop == SV_STAGE_MLP_UP) return SV_OK;
     SV_TRY(run_gemm(p.fc2[i], s));
+    if (last && stop == SV_STAGE_MLP_DOWN) return SV_OK;
   }
   SV_TRY(run_ln(p.X, g_w.enc_ln_g, g_w.enc_ln_b, p.Y, M, fp8, s));
+  if (stop == SV_STAGE_FINAL_LN) return SV_OK;
   return run_map(p.map, B, fp8, out, s);
 }
 
@@ -733,6 +746,20 @@ sv_status map_weights_view(MapWeightsView* v) {
 int* dev_err() { return g_rt.dev_err; }
 int num_sms() { return g_rt.sms; }
 
+LaunchScope::LaunchScope(int kind, double flops, double bytes, cudaStream_t s) : on_(g_prof_on) {
+  ++g_launches;
+  if (on_) {
+    ProfRec r{kind, flops, bytes, get_event(), get_event()};
+    cudaEventRecord(r.e0, s);
+    g_prof.push_back(r);
+    stream_ = s;
+  }
+}
+
+LaunchScope::~LaunchScope() {
+  if (on_) cudaEventRecord(g_prof.back().e1, stream_);
+}
+
 }  // namespace sv
 
 using namespace sv;
@@ -773,6 +800,72 @@ sv_status sv_model_dims(int* tokens, int* patch_dim, int* width, int* heads, int
   return SV_OK;
 }
 
+size_t sv_weights_count(void) {
+  if (!g_w.ready) return 0;
+  size_t n = 0;
+  for (const TensorRec& t : g_w.tensors) n += size_t(t.rows) * size_t(t.cols);
+  return n;
+}
+
+size_t sv_weights_count_e4m3(void) {
+  if (!g_w.ready) return 0;
+  size_t n = 0;
+  for (const TensorRec& t : g_w.tensors)
+    if (t.p8) n += size_t(t.rows) * size_t(t.cols);
+  return n;
+}
+
+sv_status sv_export_weights(float* host_dst, size_t n_floats) {
+  SV_TRY(check_ready());
+  const size_t need = sv_weights_count();
+  if (!host_dst || n_floats < need) {
+    set_error("sv_export_weights: needs a host buffer of %zu floats (got %zu)", need, n_floats);
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_CHECK_CUDA(cudaDeviceSynchronize(), "sv_export_weights");
+  std::vector<uint16_t> h;
+  float* dst = host_dst;
+  for (const TensorRec& t : g_w.tensors) {
+    // a dense weight is resident as [N, kpad] (K-major); the logical layout is [K, N]
+    const size_t stored = t.matrix ? size_t(t.cols) * size_t(t.kpad) : size_t(t.rows) * size_t(t.cols);
+    h.resize(stored);
+    SV_CHECK_CUDA(cudaMemcpy(h.data(), t.p16, 2 * stored, cudaMemcpyDeviceToHost), "sv_export_weights copy");
+    for (int r = 0; r < t.rows; ++r)
+      for (int c = 0; c < t.cols; ++c) {
+        const uint16_t bits = t.matrix ? h[size_t(c) * size_t(t.kpad) + size_t(r)] : h[size_t(r) * size_t(t.cols) + size_t(c)];
+        __half_raw raw;
+        raw.x = bits;
+        dst[size_t(r) * size_t(t.cols) + size_t(c)] = __half2float(__half(raw));
+      }
+    dst += size_t(t.rows) * size_t(t.cols);
+  }
+  return SV_OK;
+}
+
+sv_status sv_export_weights_e4m3(uint8_t* host_dst, size_t n_bytes) {
+  SV_TRY(check_ready());
+  const size_t need = sv_weights_count_e4m3();
+  if (!host_dst || n_bytes < need) {
+    set_error("sv_export_weights_e4m3: needs a host buffer of %zu bytes (got %zu)", need, n_bytes);
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_CHECK_CUDA(cudaDeviceSynchronize(), "sv_export_weights_e4m3");
+  std::vector<uint8_t> h;
+  uint8_t* dst = host_dst;
+  for (const TensorRec& t : g_w.tensors) {
+    if (!t.p8) continue;
+    const size_t stored = t.matrix ? size_t(t.cols) * size_t(t.kpad) : size_t(t.rows) * size_t(t.cols);
+    h.resize(stored);
+    SV_CHECK_CUDA(cudaMemcpy(h.data(), t.p8, stored, cudaMemcpyDeviceToHost), "sv_export_weights_e4m3 copy");
+    for (int r = 0; r < t.rows; ++r)
+      for (int c = 0; c < t.cols; ++c)
+        dst[size_t(r) * size_t(t.cols) + size_t(c)] =
+            t.matrix ? h[size_t(c) * size_t(t.kpad) + size_t(r)] : h[size_t(r) * size_t(t.cols) + size_t(c)];
+    dst += size_t(t.rows) * size_t(t.cols);
+  }
+  return SV_OK;
+}
+
 sv_status sv_encode_ex(const void* pixels, void* out, int batch, int layers, int gemm_dtype, int flags,
                        void* stream) {
   SV_TRY(check_ready());
@@ -803,7 +896,8 @@ sv_status sv_encode(const void* pixels, void* out, int batch, int layers, int ge
 
 sv_status sv_gemm_bias_act(const void* A, const void* W, const void* bias, const void* pos, int pos_rows,
                            const void* residual, void* C, int M, int N, int K, int act, int in_dtype, int out_dtype,
-                           float scale, void* stream) {
+                           float scale_a, float scale_w, void* stream) {
+  const float scale = scale_a * scale_w;
   if (!A || !W || !C || M < 1 || N < 16 || K < 16 || N % 16 || K % 16 || (act != 0 && act != 1) ||
       (in_dtype != 0 && in_dtype != 1) || (out_dtype != 0 && out_dtype != 1) || (pos && pos_rows < 1) ||
       !std::isfinite(scale)) {
@@ -902,20 +996,25 @@ sv_status sv_pack_patches(const void* images, void* pixels, int batch, int image
                              channels, patch, s);
 }
 
-sv_status sv_layernorm(const void* x, const void* gamma, const void* beta, void* y, int rows, int width, float eps,
-                       int out_dtype, void* stream) {
+sv_status sv_layernorm(void* x, const void* residual, const void* gamma, const void* beta, void* y, int rows,
+                       int width, float eps, int out_dtype, void* stream) {
   if (!x || !gamma || !beta || !y || rows < 1 || width < 8 || width > 4096 || width % 8 || !(eps >= 0.0f) ||
       (out_dtype != 0 && out_dtype != 1)) {
     set_error("sv_layernorm: bad arguments (rows %d, width %d)", rows, width);
     return SV_ERR_INVALID_ARG;
   }
-  if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(beta, 16) || !aligned(y, 16)) {
+  if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(gamma, 16) || !aligned(beta, 16) || !aligned(y, 16)) {
     set_error("sv_layernorm: pointers must be 16-byte aligned");
     return SV_ERR_INVALID_ARG;
   }
   SV_TRY(ensure_runtime());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  Launch L(kKindLN, 8.0 * rows * width, double(rows) * width * (2.0 + (out_dtype ? 1.0 : 2.0)), s);
+  const double rb = residual ? 4.0 : 0.0;  // the residual read and the sum written back
+  Launch L(kKindLN, 8.0 * rows * width, double(rows) * width * (2.0 + rb + (out_dtype ? 1.0 : 2.0)), s);
+  if (residual)
+    return layernorm_residual_launch(static_cast<__half*>(x), static_cast<const __half*>(residual),
+                                     static_cast<const __half*>(gamma), static_cast<const __half*>(beta), y, rows,
+                                     width, eps, out_dtype, s);
   return layernorm_launch(static_cast<const __half*>(x), static_cast<const __half*>(gamma),
                           static_cast<const __half*>(beta), y, rows, width, eps, out_dtype, s);
 }
@@ -925,47 +1024,97 @@ sv_status sv_attention(const void* qkv, void* o, int batch, int heads, int token
   return sv_attention_ex(qkv, o, batch, heads, tokens, head_dim, scale, out_dtype, 0, stream);
 }
 
-sv_status sv_attention_ex(const void* qkv, void* o, int batch, int heads, int tokens, int head_dim, float scale,
-                          int out_dtype, int flags, void* stream) {
-  if (!qkv || !o || batch < 1 || heads < 1 || tokens < 1 || batch > 65535 || !std::isfinite(scale) ||
+}  // extern "C"
+
+namespace sv {
+namespace {
+// Shared checks of the attention entry points, and their scratch buffer: the
+// head-blocked copy of the operands, grown to the largest call, freed by sv_shutdown.
+sv_status attention_args(const char* fn, const void* o, int batch, int heads, int tokens, int head_dim, float* scale,
+                         int out_dtype, int flags) {
+  if (!o || batch < 1 || heads < 1 || tokens < 1 || batch > 65535 || !std::isfinite(*scale) ||
       (out_dtype != 0 && out_dtype != 1) || (flags & ~SV_ATTENTION_QK_E4M3)) {
-    set_error("sv_attention: bad arguments");
+    set_error("%s: bad arguments", fn);
     return SV_ERR_INVALID_ARG;
   }
   if (head_dim != 72) {
-    set_error("sv_attention: head_dim %d is not supported (72 only)", head_dim);
+    set_error("%s: head_dim %d is not supported (72 only)", fn, head_dim);
     return SV_ERR_UNSUPPORTED;
   }
-  if (!aligned(qkv, 16) || !aligned(o, 16)) {
-    set_error("sv_attention: pointers must be 16-byte aligned");
+  if (!aligned(o, 16)) {
+    set_error("%s: pointers must be 16-byte aligned", fn);
+    return SV_ERR_INVALID_ARG;
+  }
+  if (*scale <= 0.0f) *scale = 1.0f / std::sqrt(float(head_dim));  // scaled dot-product attention
+  return SV_OK;
+}
+
+sv_status attention_scratch(size_t need, const char* fn) {
+  if (need <= g_attn_scratch_bytes) return SV_OK;
+  if (g_attn_scratch) {
+    SV_CHECK_CUDA(cudaDeviceSynchronize(), fn);
+    cudaFree(g_attn_scratch);
+    g_attn_scratch = nullptr;
+    g_attn_scratch_bytes = 0;
+  }
+  cudaError_t e = cudaMalloc(&g_attn_scratch, need);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_error("%s: cudaMalloc of %zu bytes failed", fn, need);
+    return SV_ERR_OOM;
+  }
+  g_attn_scratch_bytes = need;
+  return SV_OK;
+}
+
+sv_status attention_on_scratch(void* o, int batch, int heads, int tokens, float scale, int out_dtype, int flags,
+                               cudaStream_t s) {
+  Launch L(kKindAttn, 4.0 * batch * heads * double(tokens) * tokens * 72.0, 0.0, s);
+  return attention_launch(g_attn_scratch, o, batch, tokens, heads, scale, out_dtype, flags & SV_ATTENTION_QK_E4M3,
+                          s);
+}
+}  // namespace
+}  // namespace sv
+
+extern "C" {
+
+sv_status sv_attention_ex(const void* qkv, void* o, int batch, int heads, int tokens, int head_dim, float scale,
+                          int out_dtype, int flags, void* stream) {
+  SV_TRY(attention_args("sv_attention", o, batch, heads, tokens, head_dim, &scale, out_dtype, flags));
+  if (!qkv || !aligned(qkv, 16)) {
+    set_error("sv_attention: qkv must be a 16-byte aligned pointer");
     return SV_ERR_INVALID_ARG;
   }
   SV_TRY(ensure_runtime());
-  const size_t need = attention_blocked_bytes(batch, tokens, heads);
-  if (need > g_attn_scratch_bytes) {  // grows monotonically; freed by sv_shutdown
-    if (g_attn_scratch) {
-      SV_CHECK_CUDA(cudaDeviceSynchronize(), "sv_attention");
-      cudaFree(g_attn_scratch);
-      g_attn_scratch = nullptr;
-      g_attn_scratch_bytes = 0;
-    }
-    cudaError_t e = cudaMalloc(&g_attn_scratch, need);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      set_error("sv_attention: cudaMalloc of %zu bytes failed", need);
-      return SV_ERR_OOM;
-    }
-    g_attn_scratch_bytes = need;
-  }
+  SV_TRY(attention_scratch(attention_blocked_bytes(batch, tokens, heads), "sv_attention"));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   {
     Launch L(kKindOther, 0.0, double(batch) * tokens * 3 * heads * 72 * 4.0, s);
     SV_TRY(attention_repack_launch(static_cast<const __half*>(qkv), g_attn_scratch, batch, tokens, heads,
                                    flags & SV_ATTENTION_QK_E4M3, s));
   }
-  Launch L(kKindAttn, 4.0 * batch * heads * double(tokens) * tokens * 72.0, 0.0, s);
-  return attention_launch(g_attn_scratch, o, batch, tokens, heads, scale, out_dtype, flags & SV_ATTENTION_QK_E4M3,
-                          s);
+  return attention_on_scratch(o, batch, heads, tokens, scale, out_dtype, flags, s);
+}
+
+sv_status sv_attention_heads(const void* q, const void* k, const void* v, void* o, int batch, int heads, int tokens,
+                             int head_dim, int head_stride, float scale, int out_dtype, int flags, void* stream) {
+  SV_TRY(attention_args("sv_attention_heads", o, batch, heads, tokens, head_dim, &scale, out_dtype, flags));
+  if (!q || !k || !v || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || head_stride < head_dim ||
+      head_stride % 8 || head_stride > 4096) {
+    set_error("sv_attention_heads: q, k, v must be 16-byte aligned and head_stride (%d) a multiple of 8 in "
+              "[head_dim, 4096]", head_stride);
+    return SV_ERR_INVALID_ARG;
+  }
+  SV_TRY(ensure_runtime());
+  SV_TRY(attention_scratch(attention_blocked_bytes(batch, tokens, heads), "sv_attention_heads"));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    Launch L(kKindOther, 0.0, double(batch) * tokens * 3 * heads * 72 * 4.0, s);
+    SV_TRY(attention_repack_heads_launch(static_cast<const __half*>(q), static_cast<const __half*>(k),
+                                         static_cast<const __half*>(v), g_attn_scratch, batch, tokens, heads,
+                                         head_stride, flags & SV_ATTENTION_QK_E4M3, s));
+  }
+  return attention_on_scratch(o, batch, heads, tokens, scale, out_dtype, flags, s);
 }
 
 sv_status sv_map_pool(const void* x, void* out, int batch, int gemm_dtype, void* stream) {
@@ -1123,8 +1272,55 @@ sv_status sv_debug_wait_timeout(unsigned int limit_us, void* stream) {
   return wait_probe_launch(limit_us, s);
 }
 
+sv_status sv_debug_encode_stage(const void* pixels, int batch, int layers, int gemm_dtype, int flags, int stage,
+                                void* dst, size_t dst_bytes, void* stream) {
+  SV_TRY(check_ready());
+  const Dims& d = g_w.d;
+  if (!pixels || !dst || batch < 1 || layers < 1 || layers > d.L || stage < SV_STAGE_PATCH ||
+      stage > SV_STAGE_FINAL_LN || (gemm_dtype != SV_GEMM_F16 && gemm_dtype != SV_GEMM_E4M3) ||
+      (flags & ~(SV_ENCODE_UNFUSED_QKV | SV_ENCODE_FP8_ATTENTION | SV_ENCODE_EAGER)) || !aligned(pixels, 8) ||
+      !aligned(dst, 16)) {
+    set_error("sv_debug_encode_stage: bad arguments");
+    return SV_ERR_INVALID_ARG;
+  }
+  if (stage == SV_STAGE_QKV && (flags & SV_ENCODE_FP8_ATTENTION)) {
+    set_error("sv_debug_encode_stage: the QKV stage with E4M3 Q and K is not supported");
+    return SV_ERR_UNSUPPORTED;
+  }
+  const size_t M = size_t(batch) * d.T, eb = gemm_dtype == SV_GEMM_E4M3 ? 1 : 2;
+  size_t bytes = 0;
+  switch (stage) {
+    case SV_STAGE_PATCH:
+    case SV_STAGE_OUT_PROJ:
+    case SV_STAGE_MLP_DOWN: bytes = M * d.D * 2; break;
+    case SV_STAGE_QKV: bytes = M * 3 * d.D * 2; break;
+    case SV_STAGE_ATTENTION:
+    case SV_STAGE_FINAL_LN: bytes = M * d.D * eb; break;
+    default: bytes = M * d.F * eb; break;  // SV_STAGE_MLP_UP
+  }
+  if (dst_bytes < bytes) {
+    set_error("sv_debug_encode_stage: stage %d needs %zu bytes (got %zu)", stage, bytes, dst_bytes);
+    return SV_ERR_INVALID_ARG;
+  }
+  Plan* p = nullptr;
+  SV_TRY(get_plan(batch, gemm_dtype, flags & ~SV_ENCODE_EAGER, &p));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SV_TRY(encode(*p, static_cast<const __half*>(pixels), nullptr, layers, s, stage));
+  const void* src = stage == SV_STAGE_ATTENTION ? p->O
+                    : stage == SV_STAGE_MLP_UP  ? p->Hh
+                    : stage == SV_STAGE_FINAL_LN ? p->Y
+                                                 : static_cast<const void*>(p->X);
+  if (stage == SV_STAGE_QKV) {
+    Launch L(kKindOther, 0.0, double(bytes) * 2.0, s);
+    return attention_unpack_launch(p->QKV, static_cast<__half*>(dst), batch, d.T, d.H, s);
+  }
+  SV_CHECK_CUDA(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s), "sv_debug_encode_stage copy");
+  return SV_OK;
+}
+
 void sv_shutdown(void) {
   if (g_rt.ready) cudaDeviceSynchronize();
+  map_static_forget();
   free_weights();
   for (const ProfRec& r : g_prof) {
     cudaEventDestroy(r.e0);

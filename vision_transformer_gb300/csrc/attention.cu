@@ -572,21 +572,12 @@ __global__ void __maxnreg__(168) attention_kernel(const Params p) {
   }
 }
 
-// Row-major [B, T, 3 D] -> head-blocked; one thread per 16-byte group of 8 values.
-// qk8: Q and K as E4M3(16 x), 8 bytes per group (the head's last group also writes the
-// zero pad of its 16-value group).
-__global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restrict__ blk, int B, int T, int H,
-                              int tiles, int qk8) {
-  const int D = H * kDh;
-  const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long per_row = 3L * D / 8;
-  if (i >= long(B) * T * per_row) return;
-  const long m = i / per_row;
-  const int col = int(i - m * per_row) * 8;
-  const int bimg = int(m / T), t = int(m - long(bimg) * T);
-  const int which = col / D, rem = col - which * D, h = rem / kDh, cg = (rem - h * kDh) >> 3;
+// One 16-byte group of 8 values (column group cg of head h, token t of image b) into
+// the head-blocked layout; qk8: Q and K as E4M3(16 x), 8 bytes per group (the head's
+// last group also writes the zero pad of its 16-value group).
+__device__ __forceinline__ void store_blocked(uint8_t* blk, int which, int bimg, int h, int t, int cg, const uint4& u,
+                                              int qk8, int B, int H, int tiles) {
   const size_t idx = ((size_t(which) * B + bimg) * H + h) * tiles + (t >> 7);
-  const uint4 u = *reinterpret_cast<const uint4*>(qkv + m * 3 * D + col);
   uint8_t* dst = blk + idx * kBlockBytes + (t & 127) * 16;
   if (qk8 && which < 2) {
     const __half2* hv = reinterpret_cast<const __half2*>(&u);
@@ -607,6 +598,57 @@ __global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restric
   *reinterpret_cast<uint4*>(dst + cg * kGroupBytes) = u;
 }
 
+// Row-major [B, T, 3 D] -> head-blocked; one thread per 16-byte group of 8 values.
+__global__ void repack_kernel(const __half* __restrict__ qkv, uint8_t* __restrict__ blk, int B, int T, int H,
+                              int tiles, int qk8) {
+  const int D = H * kDh;
+  const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long per_row = 3L * D / 8;
+  if (i >= long(B) * T * per_row) return;
+  const long m = i / per_row;
+  const int col = int(i - m * per_row) * 8;
+  const int bimg = int(m / T), t = int(m - long(bimg) * T);
+  const int which = col / D, rem = col - which * D, h = rem / kDh, cg = (rem - h * kDh) >> 3;
+  const uint4 u = *reinterpret_cast<const uint4*>(qkv + m * 3 * D + col);
+  store_blocked(blk, which, bimg, h, t, cg, u, qk8, B, H, tiles);
+}
+
+// Per-head q, k, v [B, H, T, stride] (the first 72 values of a row) -> head-blocked;
+// one thread per 16-byte group of 8 values.
+__global__ void repack_heads_kernel(const __half* __restrict__ q, const __half* __restrict__ k,
+                                    const __half* __restrict__ v, uint8_t* __restrict__ blk, int B, int T, int H,
+                                    int stride, int tiles, int qk8) {
+  const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long per_which = long(B) * H * T * kGroups;
+  if (i >= 3 * per_which) return;
+  const int which = int(i / per_which);
+  long r = i - which * per_which;
+  const int cg = int(r % kGroups);
+  r /= kGroups;  // ((b H + h) T + t)
+  const int t = int(r % T);
+  const long bh = r / T;
+  const int h = int(bh % H), bimg = int(bh / H);
+  const __half* src = which == 0 ? q : (which == 1 ? k : v);
+  const uint4 u = *reinterpret_cast<const uint4*>(src + r * stride + cg * 8);
+  store_blocked(blk, which, bimg, h, t, cg, u, qk8, B, H, tiles);
+}
+
+// Head-blocked F16 Q, K, V -> row-major [B, T, 3 D]; one thread per 16-byte group.
+__global__ void unpack_kernel(const uint8_t* __restrict__ blk, __half* __restrict__ qkv, int B, int T, int H,
+                              int tiles) {
+  const int D = H * kDh;
+  const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long per_row = 3L * D / 8;
+  if (i >= long(B) * T * per_row) return;
+  const long m = i / per_row;
+  const int col = int(i - m * per_row) * 8;
+  const int bimg = int(m / T), t = int(m - long(bimg) * T);
+  const int which = col / D, rem = col - which * D, h = rem / kDh, cg = (rem - h * kDh) >> 3;
+  const size_t idx = ((size_t(which) * B + bimg) * H + h) * tiles + (t >> 7);
+  *reinterpret_cast<uint4*>(qkv + m * 3 * D + col) =
+      *reinterpret_cast<const uint4*>(blk + idx * kBlockBytes + (t & 127) * 16 + cg * kGroupBytes);
+}
+
 // Buffer configuration launched: one Q staging buffer (both tiles of an item; the
 // next item's queries arrive in it during the current item) and 3 + 3 K / V stages.
 template <int QB, int KS, int VS, bool QK8>
@@ -618,8 +660,8 @@ sv_status attention_launch_cfg(const Params& p, int grid, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice(attention)");
-  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-  if (!(attr_set & bit)) {
+  const unsigned long long bit = (dev >= 0 && dev < kMaxAttrDevices) ? 1ull << dev : 0ull;
+  if (!(attr_set & bit) || !bit) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
     attr_set |= bit;
@@ -641,6 +683,23 @@ sv_status attention_repack_launch(const __half* qkv, void* blocked, int B, int T
                                                            (T + kTile - 1) / kTile, qk8);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "attention repack launch");
+}
+
+sv_status attention_repack_heads_launch(const __half* q, const __half* k, const __half* v, void* blocked, int B,
+                                        int T, int H, int stride, int qk8, cudaStream_t s) {
+  const long n = 3L * B * H * T * kGroups;
+  repack_heads_kernel<<<unsigned((n + 255) / 256), 256, 0, s>>>(q, k, v, static_cast<uint8_t*>(blocked), B, T, H,
+                                                                 stride, (T + kTile - 1) / kTile, qk8);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "attention repack (per head) launch");
+}
+
+sv_status attention_unpack_launch(const void* blocked, __half* qkv, int B, int T, int H, cudaStream_t s) {
+  const long n = long(B) * T * (3L * H * kDh / 8);
+  unpack_kernel<<<unsigned((n + 255) / 256), 256, 0, s>>>(static_cast<const uint8_t*>(blocked), qkv, B, T, H,
+                                                          (T + kTile - 1) / kTile);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "attention unpack launch");
 }
 
 sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, float scale, int out_e4m3, int qk8,

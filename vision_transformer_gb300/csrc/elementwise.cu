@@ -29,7 +29,9 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 // mean, then the centred (biased) variance, both in F32 from the row held in
 // registers, then the affine map. Each of the 16 lanes owns CPL chunks of 8 values
 // (16-byte loads, all issued before any arithmetic); a 1152-wide row is 9 chunks
-// per lane. With `stats_r` set only the row statistics are written:
+// per lane. With `res` set the row is first x + res (LayerNorm/Add paragraph: the
+// residual add before the normalisation), added in F32 and rounded to F16 once; that
+// sum is stored to x_out and normalised. With `stats_r` set only the row statistics are written:
 // 1/sqrt(var + eps) to stats_r and, for the consuming GEMM's extra K block, the F16
 // row (-mean_hi, -mean_hi, -mean_lo, 0...) to stats_aug (mean_hi + mean_lo = mean to
 // about 2^-22 relative).
@@ -40,7 +42,8 @@ __device__ __forceinline__ float half_sum(float v) {  // over the 16 lanes of a 
 }
 
 template <int CPL>
-__global__ void __launch_bounds__(256, CPL <= 9 ? 4 : 1) layernorm_kernel(const __half* __restrict__ x, const __half* __restrict__ g,
+__global__ void __launch_bounds__(256, CPL <= 9 ? 4 : 1) layernorm_kernel(const __half* x, const __half* __restrict__ res,
+                                                        __half* x_out, const __half* __restrict__ g,
                                                         const __half* __restrict__ bta, void* __restrict__ y,
                                                         int rows, int width, float eps, int out_e4m3,
                                                         float* __restrict__ stats_r, __half* __restrict__ stats_aug) {
@@ -56,7 +59,25 @@ __global__ void __launch_bounds__(256, CPL <= 9 ? 4 : 1) layernorm_kernel(const 
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
     const int c = hl + 16 * i;
-    u[i] = c < chunks ? __ldg(reinterpret_cast<const uint4*>(xr) + c) : make_uint4(0u, 0u, 0u, 0u);
+    u[i] = c < chunks ? *(reinterpret_cast<const uint4*>(xr) + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (res) {  // x + res, rounded to F16, written back (each lane its own chunks)
+    const __half* rr = res + row * long(width);
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = hl + 16 * i;
+      if (c < chunks) {
+        const uint4 ru = __ldg(reinterpret_cast<const uint4*>(rr) + c);
+        __half2* xh = reinterpret_cast<__half2*>(&u[i]);
+        const __half2* rh = reinterpret_cast<const __half2*>(&ru);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 a = __half22float2(xh[k]), b = __half22float2(rh[k]);
+          xh[k] = __floats2half2_rn(a.x + b.x, a.y + b.y);
+        }
+        if (live) *(reinterpret_cast<uint4*>(x_out + row * long(width)) + c) = u[i];
+      }
+    }
   }
   float s = 0.0f;
 #pragma unroll
@@ -428,25 +449,25 @@ __global__ void __launch_bounds__(256) fold_ln_kernel(__half* __restrict__ W, co
 }
 
 template <int CPL>
-void ln_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width, float eps,
-               int out_e4m3, float* stats_r, __half* stats_aug, cudaStream_t s) {
+void ln_launch(const __half* x, const __half* res, __half* x_out, const __half* g, const __half* b, void* y, int rows,
+               int width, float eps, int out_e4m3, float* stats_r, __half* stats_aug, cudaStream_t s) {
   // a launch error stays pending for the caller's cudaGetLastError
-  launch_pdl(layernorm_kernel<CPL>, dim3(unsigned((rows + 15) / 16)), dim3(256), 0, s, x, g, b, y, rows, width, eps,
-             out_e4m3, stats_r, stats_aug);
+  launch_pdl(layernorm_kernel<CPL>, dim3(unsigned((rows + 15) / 16)), dim3(256), 0, s, x, res, x_out, g, b, y, rows,
+             width, eps, out_e4m3, stats_r, stats_aug);
 }
 
 }  // namespace
 
 namespace {
-sv_status ln_any(const __half* x, const __half* g, const __half* b, void* y, int rows, int width, float eps,
-                 int out_e4m3, float* stats_r, __half* stats_aug, cudaStream_t s) {
+sv_status ln_any(const __half* x, const __half* res, __half* x_out, const __half* g, const __half* b, void* y, int rows,
+                 int width, float eps, int out_e4m3, float* stats_r, __half* stats_aug, cudaStream_t s) {
   const int cpl = (width / 8 + 15) / 16;  // 16-byte chunks per lane of a half-warp
-  if (cpl <= 1) ln_launch<1>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
-  else if (cpl <= 2) ln_launch<2>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
-  else if (cpl <= 4) ln_launch<4>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
-  else if (cpl <= 9) ln_launch<9>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
-  else if (cpl <= 16) ln_launch<16>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
-  else if (cpl <= 32) ln_launch<32>(x, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  if (cpl <= 1) ln_launch<1>(x, res, x_out, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 2) ln_launch<2>(x, res, x_out, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 4) ln_launch<4>(x, res, x_out, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 9) ln_launch<9>(x, res, x_out, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 16) ln_launch<16>(x, res, x_out, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
+  else if (cpl <= 32) ln_launch<32>(x, res, x_out, g, b, y, rows, width, eps, out_e4m3, stats_r, stats_aug, s);
   else {
     set_error("layernorm: width %d too large", width);
     return SV_ERR_UNSUPPORTED;
@@ -458,12 +479,17 @@ sv_status ln_any(const __half* x, const __half* g, const __half* b, void* y, int
 
 sv_status layernorm_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width,
                            float eps, int out_e4m3, cudaStream_t s) {
-  return ln_any(x, g, b, y, rows, width, eps, out_e4m3, nullptr, nullptr, s);
+  return ln_any(x, nullptr, nullptr, g, b, y, rows, width, eps, out_e4m3, nullptr, nullptr, s);
+}
+
+sv_status layernorm_residual_launch(__half* x, const __half* res, const __half* g, const __half* b, void* y, int rows,
+                                    int width, float eps, int out_e4m3, cudaStream_t s) {
+  return ln_any(x, res, x, g, b, y, rows, width, eps, out_e4m3, nullptr, nullptr, s);
 }
 
 sv_status ln_stats_launch(const __half* x, float* stats_r, __half* stats_aug, int rows, int width, float eps,
                           cudaStream_t s) {
-  return ln_any(x, nullptr, nullptr, nullptr, rows, width, eps, 0, stats_r, stats_aug, s);
+  return ln_any(x, nullptr, nullptr, nullptr, nullptr, nullptr, rows, width, eps, 0, stats_r, stats_aug, s);
 }
 
 sv_status ln_finalize_launch(const float2* part, int tiles, int tile_w, float* r, __half* aug, int rows, int width,
@@ -520,11 +546,15 @@ sv_status wait_probe_launch(unsigned int limit_us, cudaStream_t s) {
 sv_status map_attn_launch(const __half* q, const __half* kv, void* out, int B, int T, int H, float scale,
                           int out_e4m3, cudaStream_t s) {
   const size_t smem = sizeof(float) * (size_t(T) + size_t(kMapKeyGroups) * 72);
-  static size_t attr = 0;
-  if (smem > 48 * 1024 && smem > attr) {
+  // the attribute is per device: the largest value set so far on each device
+  static size_t attr[kMaxAttrDevices] = {};
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return cuda_fail(de, "cudaGetDevice(map_attn)");
+  if (smem > 48 * 1024 && (dev < 0 || dev >= kMaxAttrDevices || smem > attr[dev])) {
     cudaError_t e = cudaFuncSetAttribute(map_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(map_attn)");
-    attr = smem;
+    if (dev >= 0 && dev < kMaxAttrDevices) attr[dev] = smem;
   }
   cudaError_t e = launch_pdl(map_attn_kernel, dim3(unsigned(H), unsigned(B)), dim3(kMapThreads), smem, s, q, kv, out, T,
                              H * 72, scale * 1.4426950408889634f, out_e4m3);

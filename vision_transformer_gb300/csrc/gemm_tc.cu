@@ -666,12 +666,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, bool FP8, bool PAIR, int ATOMS = 1>
 sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
   using C = Cfg<BN, PAIR, ATOMS>;
-  static bool attr_set = false;
   auto kern = gemm_tc_kernel<BN, FP8, PAIR, ATOMS>;
-  if (!attr_set) {
+  // the attribute is per device: set it once on each device the kernel runs on
+  static unsigned long long attr_set = 0;
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return cuda_fail(de, "cudaGetDevice(gemm)");
+  const unsigned long long bit = (dev >= 0 && dev < kMaxAttrDevices) ? 1ull << dev : 0ull;
+  if (!(attr_set & bit) || !bit) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm)");
-    attr_set = true;
+    attr_set |= bit;
   }
   const int items = PAIR ? ((prm.m_tiles + 1) / 2) * prm.n_tiles : prm.m_tiles * prm.n_tiles;
   const int slots = PAIR ? num_sms() / 2 : num_sms();  // one CTA (PAIR: one two-CTA cluster) per SM (pair)

@@ -6,14 +6,18 @@
 // allocator, a memory pool sized up front), code running under a strict
 // memory budget, or code that must not block on the driver's allocator while
 // other work is in flight. This variant runs the same head with its scratch in
-// one fixed array compiled into the library (kStaticScratchBytes). Every GPU
-// that loads the library holds that array until the process exits.
+// one fixed array compiled into the library (kStaticScratchBytes). The array
+// takes device memory once this file's code is loaded into a device's context
+// (under CUDA's default lazy loading: at the first call of this entry point on
+// that device) and keeps it until the context is destroyed.
 //
 // The array's host-side name is not a device address. The first call on a
 // device asks the runtime for the array's device address with
 // cudaGetSymbolAddress (with that device current) and keeps it; only that
 // address is handed to kernels. The first call on a device should therefore
-// come before any stream capture on that device.
+// come before any stream capture on that device. sv_shutdown forgets the kept
+// addresses (map_static_forget), so a context destroyed after sv_shutdown is
+// looked up anew.
 //
 // All calls share the one array and it keeps the previous call's contents;
 // every buffer in it is written before it is read within a call, so nothing
@@ -84,6 +88,15 @@ sv_status scratch_address(char** out) {
   return SV_OK;
 }
 
+// One GEMM launch with its accounting (launch count, profile records).
+sv_status run(const GemmOperands& g, const GemmEpi& e, int k_logical, cudaStream_t s) {
+  const double eb = g.fp8 ? 1.0 : 2.0;
+  double bytes = (double(g.M) + double(g.N)) * k_logical * eb + double(g.M) * g.N * (e.out_e4m3 ? 1.0 : 2.0);
+  if (e.residual) bytes += double(g.M) * g.N * 2.0;
+  LaunchScope L(kKindGemm, 2.0 * g.M * double(g.N) * double(k_logical), bytes, s);
+  return gemm_launch(g, e, s);
+}
+
 #define SV_TRY_S(call)          \
   do {                          \
     sv_status s_ = (call);      \
@@ -91,6 +104,11 @@ sv_status scratch_address(char** out) {
   } while (0)
 
 }  // namespace
+
+void map_static_forget() {
+  for (void*& p : g_scratch_dev) p = nullptr;
+}
+
 }  // namespace sv
 
 using namespace sv;
@@ -137,13 +155,14 @@ extern "C" sv_status sv_map_pool_static(const void* x, void* out, int batch, int
   e.bias = w.q_b;
   e.out = q;
   SV_TRY_S(gemm_bind_epilogue(&g, e));
-  SV_TRY_S(gemm_launch(g, e, st));
+  SV_TRY_S(run(g, e, w.D, st));
   // one image at a time: [K V] = x_b . Wkv + bkv, then the single-query attention into a[b]
   const size_t img = size_t(w.T) * w.D;
   for (int b = 0; b < batch; ++b) {
     const __half* xb = static_cast<const __half*>(x) + size_t(b) * img;
     const void* A_op = xb;
     if (fp8) {
+      LaunchScope L(kKindOther, 0.0, double(img) * 3.0, st);
       SV_TRY_S(quantize_launch(xb, x8, img, st));
       A_op = x8;
     }
@@ -151,7 +170,8 @@ extern "C" sv_status sv_map_pool_static(const void* x, void* out, int batch, int
     e.bias = w.kv_b;
     e.out = kv;
     SV_TRY_S(gemm_bind_epilogue(&g, e));
-    SV_TRY_S(gemm_launch(g, e, st));
+    SV_TRY_S(run(g, e, w.D, st));
+    LaunchScope L(kKindMapAttn, 4.0 * w.T * double(w.D), double(w.T) * 2 * w.D * 2.0, st);
     SV_TRY_S(map_attn_launch(q, kv, static_cast<char*>(a) + size_t(b) * w.D * eb, 1, w.T, w.H, attn_scale, fp8,
                              st));
   }
@@ -160,15 +180,18 @@ extern "C" sv_status sv_map_pool_static(const void* x, void* out, int batch, int
   e.bias = w.out_b;
   e.out = A;
   SV_TRY_S(gemm_bind_epilogue(&g, e));
-  SV_TRY_S(gemm_launch(g, e, st));
-  SV_TRY_S(layernorm_launch(A, w.ln_g, w.ln_b, Ya, batch, w.D, 1e-6f, fp8, st));
+  SV_TRY_S(run(g, e, w.D, st));
+  {
+    LaunchScope L(kKindLN, 8.0 * batch * w.D, double(batch) * w.D * 3.0, st);
+    SV_TRY_S(layernorm_launch(A, w.ln_g, w.ln_b, Ya, batch, w.D, 1e-6f, fp8, st));
+  }
   SV_TRY_S(gemm_prepare(&g, Ya, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, batch, w.F, w.D, fp8));
   e.bias = w.fc1_b;
   e.act = SV_ACT_GELU_TANH;
   e.out_e4m3 = fp8;
   e.out = Ha;
   SV_TRY_S(gemm_bind_epilogue(&g, e));
-  SV_TRY_S(gemm_launch(g, e, st));
+  SV_TRY_S(run(g, e, w.D, st));
   SV_TRY_S(gemm_prepare(&g, Ha, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, batch, w.D, w.F, fp8));
   e.bias = w.fc2_b;
   e.act = SV_ACT_NONE;
@@ -176,5 +199,5 @@ extern "C" sv_status sv_map_pool_static(const void* x, void* out, int batch, int
   e.residual = A;
   e.out = out;
   SV_TRY_S(gemm_bind_epilogue(&g, e));
-  return gemm_launch(g, e, st);
+  return run(g, e, w.F, st);
 }

@@ -19,6 +19,29 @@ int num_sms();
 
 enum KernelKind { kKindGemm = 0, kKindAttn = 1, kKindLN = 2, kKindMapAttn = 3, kKindOther = 4, kNumKinds = 5 };
 
+// Accounting of one library launch (api.cu): counts it for sv_launch_count and,
+// while profiling is on, brackets it with CUDA events on its stream for
+// sv_profile_read. Construct it right before the launch; it closes at scope end.
+class LaunchScope {
+ public:
+  LaunchScope(int kind, double flops, double bytes, cudaStream_t s);
+  ~LaunchScope();
+  LaunchScope(const LaunchScope&) = delete;
+  LaunchScope& operator=(const LaunchScope&) = delete;
+
+ private:
+  bool on_;
+  cudaStream_t stream_ = nullptr;
+};
+
+// Kernel attributes (dynamic shared memory limits) are set once per device; device
+// ordinals at or above this bound set them on every launch.
+constexpr int kMaxAttrDevices = 64;
+
+// Forgets the device addresses sv_map_pool_static has looked up (map_static.cu);
+// called by sv_shutdown.
+void map_static_forget();
+
 // Read-only view of the resident MAP-head weights and model sizes (api.cu).
 struct MapWeightsView {
   int T, D, H, F;
@@ -125,6 +148,11 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 size_t attention_blocked_bytes(int B, int T, int H);
 // Row-major [B, T, 3*H*72] f16 -> head-blocked (qk8: Q and K quantised to E4M3).
 sv_status attention_repack_launch(const __half* qkv, void* blocked, int B, int T, int H, int qk8, cudaStream_t s);
+// Per-head q, k, v [B, H, T, stride] f16 (first 72 values of each row used) -> head-blocked.
+sv_status attention_repack_heads_launch(const __half* q, const __half* k, const __half* v, void* blocked, int B,
+                                        int T, int H, int stride, int qk8, cudaStream_t s);
+// Head-blocked F16 Q, K, V -> row-major [B, T, 3*H*72] f16 (the inverse of the repack).
+sv_status attention_unpack_launch(const void* blocked, __half* qkv, int B, int T, int H, cudaStream_t s);
 // o: [B, T, H*72] f16 / e4m3. qk8: Q and K blocks are E4M3, S = Q K^T on E4M3 operands.
 sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, float scale, int out_e4m3, int qk8,
                            cudaStream_t s);
@@ -132,6 +160,9 @@ sv_status attention_launch(const void* blocked, void* o, int B, int T, int H, fl
 // ---- elementwise (elementwise.cu)
 sv_status layernorm_launch(const __half* x, const __half* g, const __half* b, void* y, int rows, int width,
                            float eps, int out_e4m3, cudaStream_t s);
+// The same on x + res (F16 sum, written back to x).
+sv_status layernorm_residual_launch(__half* x, const __half* res, const __half* g, const __half* b, void* y, int rows,
+                                    int width, float eps, int out_e4m3, cudaStream_t s);
 // Row statistics only, for a LayerNorm folded into a GEMM: r[m] = 1/sqrt(var + eps)
 // and aug[m, 0..15] = (-mean_hi, -mean_hi, -mean_lo, 0, ...) in F16.
 sv_status ln_stats_launch(const __half* x, float* r, __half* aug, int rows, int width, float eps, cudaStream_t s);
