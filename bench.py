@@ -9,10 +9,12 @@ weights are drawn by the seeded generator and resident in HBM; pixels are
 uniform in [-1, 1].
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--dtype f16|e4m3] [--unfused-qkv]
-                  [--fp8-attention]
+                  [--fp8-attention] [--no-configs] [--no-cpu-baseline]
   python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
-Prints one JSON line (rank 0). Multi-GPU runs (torchrun, one rank per GPU)
+Prints one JSON line (rank 0). On one GPU the line also carries `configs`: the
+batch-1 and batch-32 F16 and the batch-2 and batch-128 E4M3 workloads, each timed
+in the same run after the main one, with its own warm-up and clock record. Multi-GPU runs (torchrun, one rank per GPU)
 are independent replicas on disjoint images: no collective on the data path,
 only a barrier and a max-over-ranks of the elapsed time.
 """
@@ -50,8 +52,8 @@ def flops_per_image(layers: int = L27) -> float:
 # the kernel sources it was taken on (first 16 hex digits of sha256 of each file).
 GEMM_TRAFFIC = {"batch": 32, "bytes_per_launch": 211.2e6,
                 "weight_bytes_per_launch": 7.6e6,  # mean F16 weight bytes of the four
-                "sources": {"vision_transformer_gb300/csrc/gemm_tc.cu": "2829212c950c5e35",
-                            "vision_transformer_gb300/csrc/ptx.cuh": "c14a6ba00ae37935"}}
+                "sources": {"vision_transformer_gb300/csrc/gemm_tc.cu": "b25233b97f9b6c7f",
+                            "vision_transformer_gb300/csrc/ptx.cuh": "44e75f94fe90035d"}}
 
 
 def gemm_traffic(batch: int, dtype: str):
@@ -184,33 +186,68 @@ def oracle_sample(min_seconds: float, max_images: int = 4, seed: int = 0):
 
 
 def run_reference(args, world, rank):
-    """CPU oracle arm: each step is one image through one layer + MAP, scaled to 27 layers."""
+    """CPU oracle arm: each timed step is one whole image (patch embedding, 27 layers, final
+    LayerNorm, MAP) through the oracle as it stands; the warm-up steps run one image through
+    one layer each (they only warm the host threads and caches)."""
     if rank != 0:
         return 0
     import oracle
     import synth
-    m = oracle.OracleModel.from_synth(0, synth.so400m(1))
-    pix = synth.pixels(1, 1)
+    m = oracle.OracleModel.from_synth(0, synth.so400m(L27))
+    warm = synth.pixels(1, 1)
     for _ in range(args.warmup):
-        m.encode(pix)
+        m.encode(warm, 1)
     times = []
-    for _ in range(args.steps):
+    for i in range(args.steps):
+        pix = synth.pixels(2000 + i, 1)
         t0 = time.perf_counter()
         m.encode(pix)
         times.append(time.perf_counter() - t0)
-    per_img_27 = statistics.mean(times) * L27
-    value = 1.0 / per_img_27
+    per_img = statistics.mean(times)
+    value = 1.0 / per_img
     cores = oracle.threads()
-    sample = ("1 image through 1 encoder layer + patch embedding + MAP per step, FP32 oracle with double "
-              "accumulation; step time x 27 taken as the 27-layer image time")
+    sample = (f"{args.steps} whole images, one per step (patch embedding, 27 layers, final LayerNorm, MAP), FP32 "
+              f"oracle with double accumulation, {sum(times):.1f} s; warm-up steps: one image through one layer each")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "images/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_img_27 * 1e3, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_img * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config(args, world),
             "cpu_baseline": {"value": value, "unit": "images/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "images/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+# The other configurations of the throughput sweep and the latency cases, timed in the
+# same run after the main workload (single-GPU runs): (name, batch, gemm dtype).
+EXTRA_CONFIGS = (("b1_f16", 1, "f16"), ("b2_e4m3", 2, "e4m3"), ("b32_f16", 32, "f16"), ("b128_e4m3", 128, "e4m3"))
+
+
+def time_config(vt, torch, dev, stream, batch, dtype, steps, warmup, local):
+    """Images/s and per-step latency of sv_encode for one (batch, dtype) on device-resident
+    pixels, with its own warm-up, CUDA events on the launching stream and clock record."""
+    gdt = vt.SV_GEMM_F16 if dtype == "f16" else vt.SV_GEMM_E4M3
+    pix = torch.empty(batch, T, P, dtype=torch.float16, device=dev)
+    vt.sv_make_pixels(3000, batch, pix)
+    out = torch.empty(batch, 1, D, dtype=torch.float16, device=dev)
+    for _ in range(warmup):
+        vt.sv_encode(pix, out, batch, L27, gdt, stream)
+    vt.sv_sync(stream)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with ClockSampler(local) as clk:
+        ev[0].record(stream)
+        for i in range(steps):
+            vt.sv_encode(pix, out, batch, L27, gdt, stream)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    vt.sv_sync(stream)
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    ms = ev[0].elapsed_time(ev[-1]) / steps
+    return {"batch": batch, "gemm_dtype": dtype, "value": batch / (ms / 1e3), "unit": "images/s",
+            "ms_per_step": ms, "latency_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
+                                              "max": max(step_ms)},
+            "steps": steps, "warmup": warmup, "clocks": clk.summary()}
 
 
 def config(args, world):
@@ -236,6 +273,7 @@ def main():
     ap.add_argument("--fp8-attention", action="store_true", help="scores on E4M3 Q and K (FP8 attention products)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configurations (configs key)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum CPU time of the oracle sample")
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -383,6 +421,19 @@ def main():
             "gpu_launches": launches,
             "clocks": clk.summary()}
 
+    if rank == 0 and world == 1 and not args.no_configs:
+        # the other configurations, same weights, same box, same run (one by one after the main workload)
+        peaks_all = measured_peaks()
+        extra = {}
+        for name, b, dt in EXTRA_CONFIGS:
+            if b == B and dt == args.dtype:
+                continue
+            r = time_config(vt, torch, dev, stream, b, dt, args.steps, args.warmup, local)
+            burst_c = peaks_all["bf16_tflops"] * (2.0 if dt == "e4m3" else 1.0)
+            r["fraction_of_peak"] = flops_per_image() * b / (r["ms_per_step"] / 1e3) / 1e12 / burst_c
+            r["peak_kind"] = f"{peaks_all['source']} dense bf16 burst" + (" x 2 (E4M3)" if dt == "e4m3" else "")
+            extra[name] = r
+        line["configs"] = extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, n, cores = oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": n / t, "unit": "images/s", "cores": cores, "kind": "oracle",
