@@ -237,6 +237,24 @@ def test_attention(sv, B, H, T, sharp):
     assert_close(host(o), ref, RT, RT * vmax, f"attention B{B} H{H} T{T}")
 
 
+@pytest.mark.parametrize("qk8", [0, 1])
+def test_attention_repeats_bit_identical(sv, qk8):
+    """The attention kernel's products reuse tensor-memory columns in issue order (the
+    next S product overwrites the P values the P V product reads); a race there would
+    show up as outputs that differ between identical launches. 12 launches at the batch-32
+    size (1536 work items over the persistent CTAs) must give the same bits."""
+    B, H, T = 32, 16, 729
+    D = H * 72
+    qkv = dev_f16(synth.normal(95, 1, (B, T, 3 * D)))
+    first = torch.empty(B, T, D, dtype=torch.float16, device="cuda")
+    sv.sv_attention_ex(qkv, first, B, H, T, flags=qk8)
+    o = torch.empty_like(first)
+    for _ in range(11):
+        sv.sv_attention_ex(qkv, o, B, H, T, flags=qk8)
+        sv.sv_sync()
+        assert torch.equal(o, first)
+
+
 @pytest.mark.parametrize("B,H,T,stride", [(2, 16, 729, 80), (1, 3, 200, 72), (3, 4, 300, 96), (1, 2, 1, 80)])
 def test_attention_heads(sv, B, H, T, stride):
     """Per-head Q, K, V [B, H, T, stride]: the columns past the head width are NaN and
