@@ -796,11 +796,14 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
   g->K = K;
   g->fp8 = fp8;
   g->has_aug = 0;
-  // CTA pairs (256-row tiles, half the W traffic per SM, deeper pipelines) for long
-  // K or wide N (the MLP down- and up-projections, QKV): measured on the 27-layer
-  // encoder, about 2% faster than single CTAs there and 1.5% slower on the
-  // 1152 x 1152 output projection.
-  g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && (K >= 2048 || N >= 2048);
+  // CTA pairs (256-row tiles, half the W traffic per SM, deeper pipelines) for K >= 1024
+  // or wide N (every encoder GEMM but the patch embedding). A single CTA's 128 x 256 tile
+  // moves 96 KB through shared memory per 64-wide K block (TMA writes and MMA reads of A
+  // and W), more than shared memory delivers in the block's 512 tensor cycles; a pair
+  // halves the W part. Measured on the 27-layer encoder: about 2% faster on the MLP and
+  // QKV GEMMs, and with two swizzle rows of K per stage 1% per step faster on the
+  // 1152 x 1152 output projection (batch 32 and 128).
+  g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && (K >= 1024 || N >= 2048);
   g->bn = gemm_pick_bn(M, N, K, g->mc);
   if (g->mc && g->bn > kPairMaxBn) g->bn = kPairMaxBn;
   // two swizzle rows of K per stage for 256-wide CTA-pair tiles over a short K that they
