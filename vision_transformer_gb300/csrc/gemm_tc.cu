@@ -17,8 +17,9 @@
 //               (clusters of 2) that share one M = 256 MMA (cta_group::2):
 //               each CTA stages its 128 rows of A and half of the W tile, the
 //               leader issues the MMAs, each CTA's TMEM holds its 128 rows;
-//   warps 2..9  epilogue, two warps per TMEM lane quarter taking alternate
-//               32-column chunks: tcgen05.ld of a chunk (the warp's next chunk
+//   warps 2..   epilogue, two (three for CTA pairs on E4M3 operands) warps per
+//               TMEM lane quarter taking every second (third) 32-column
+//               chunk: tcgen05.ld of a chunk (the warp's next chunk
 //               in flight during this chunk's math), fused math, the 32 x 32
 //               result block staged in swizzled shared memory and written by a
 //               TMA store; residual blocks arrive by TMA one chunk ahead; the
@@ -41,11 +42,21 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kSwzBytes = 128;  // one 128-byte swizzle row of K
-// Warp 0 loads, warp 1 issues the MMAs, warps 2 .. 9 run the epilogue: two per
-// TMEM lane quarter, each taking every other 32-column chunk of a tile (with four,
-// the epilogue of a K = 1152 tile took about as long as its main loop).
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Warp 0 loads, warp 1 issues the MMAs, the warps after them run the epilogue:
+// two per TMEM lane quarter, each taking every other 32-column chunk of a tile (with
+// four warps the epilogue of a K = 1152 tile took about as long as its main loop).
+// CTA pairs on E4M3 operands get three per quarter: their main loop over a K = 1152
+// tile takes half the time of the F16 one, the epilogue's work per tile is the same,
+// and with two per quarter the MMA of the 1152 -> 4304 MLP projection waited about
+// 30% of every tile for a free accumulator.
+template <bool FP8, bool PAIR>
+constexpr int epi_warps() {
+  return FP8 && PAIR ? 12 : 8;
+}
+template <bool FP8, bool PAIR>
+constexpr int gemm_threads() {
+  return 64 + 32 * epi_warps<FP8, PAIR>();
+}
 // Widest output tile used with CTA pairs (its TMEM: 2 x BN columns per CTA).
 constexpr int kPairMaxBn = 256;
 // Suspend limits (ns) of the mbarrier waits of each role. A waiter that polls
@@ -64,7 +75,7 @@ constexpr uint32_t kSleepEpi = 1000000;
 // barrier round trips per K) pay for CTA pairs over K = 1152 with L2-resident operands
 // (QKV, MLP up: 4-7% faster); one is better where A streams from DRAM (MLP down) or a
 // single CTA would be left with two stages (output projection).
-template <int BN, bool PAIR, int ATOMS>
+template <int BN, bool PAIR, int ATOMS, int EPI>
 struct Cfg {
   static constexpr int kAtomA = kBM * kSwzBytes;                   // one swizzle row of the A tile
   static constexpr int kAtomB = (PAIR ? BN / 2 : BN) * kSwzBytes;  // of the W tile (this CTA's rows)
@@ -76,14 +87,14 @@ struct Cfg {
   // result out)
   static constexpr int kEpiBlock = 2048;
   static constexpr int kEpiRing = 2;
-  static constexpr int kEpiBytes = kEpiWarps * kEpiRing * kEpiBlock;
-  static constexpr int kBarBytes = 320;
+  static constexpr int kEpiBytes = EPI * kEpiRing * kEpiBlock;
+  static constexpr int kBarBytes = 384;
   static constexpr int kBudget = 232448 - 1024 - kEpiBytes - kBarBytes;
   static constexpr int kStages = kBudget / kStage < 8 ? kBudget / kStage : 8;
   static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
   static constexpr int kSmem = 1024 + kStages * kStage + kEpiBytes + kBarBytes;
   static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
-  static_assert(8 * (2 * kStages + 5 + kEpiWarps * kEpiRing) + 8 <= kBarBytes, "barrier area");
+  static_assert(8 * (2 * kStages + 5 + EPI * kEpiRing) + 8 <= kBarBytes, "barrier area");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
@@ -186,13 +197,15 @@ __device__ __forceinline__ void tile_of(const Params& p, int it, int rank, int& 
 }
 
 template <int BN, bool FP8, bool PAIR, int ATOMS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmWt, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmAa,
                    const __grid_constant__ CUtensorMap tmWa, const __grid_constant__ CUtensorMap tmWat,
                    const Params p) {
-  using C = Cfg<BN, PAIR, ATOMS>;
+  constexpr int kEpiWarps = epi_warps<FP8, PAIR>();
+  constexpr int kParts = kEpiWarps / 4;  // epilogue warps per TMEM lane quarter
+  using C = Cfg<BN, PAIR, ATOMS, kEpiWarps>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + C::kStages * C::kStage;  // [epilogue warp][ring] 32 x 32 blocks
@@ -419,11 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // Epilogue: warp ew owns TMEM lanes 32*sub .. +31, i.e. rows row0 .. row0+31 of
-    // each tile, and of them the 32-column chunks c = half, half + 2, ...; each chunk is
+    // each tile, and of them the 32-column chunks c = part, part + kParts, ...; each chunk is
     // staged as a 32 x 32 block in shared memory (64-byte rows with the 64-byte swizzle
     // for F16, 32-byte rows with the 32-byte swizzle for E4M3) and written by one TMA
     // store, which also clips the M / N tails.
-    const int sub = warp & 3, ew = warp - 2, half = ew >> 2;
+    const int sub = warp & 3, ew = warp - 2, part = ew >> 2;
     // Ring of kEpiRing blocks per warp; chunk q (counted over all of this warp's chunks)
     // uses block q % kEpiRing. With a residual, the residual block of chunk q is
     // loaded there kResAhead chunks ahead, the result overwrites it in place and the
@@ -435,13 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // residual loads in flight per block, with the phase parity that completes them
     uint32_t res_issued = 0, res_par = 0;
     // prefetch cursor: next chunk whose residual is to be loaded (work item, chunk, counter)
-    int pit = it0, pc = half, pq = 0;
+    int pit = it0, pc = part, pq = 0;
     auto prefetch_upto = [&](int qmax) {  // issue residual loads for chunks pq .. qmax
       while (p.has_res && pq <= qmax && pit < num_items) {
         int mt2, nt2;
         tile_of<PAIR>(p, pit, rank, mt2, nt2);
         if (pc >= tile_chunks(p, nt2, BN)) {  // no (more) chunks of this warp in the tile
-          pc = half;
+          pc = part;
           pit += it_step;
           continue;
         }
@@ -456,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       mt2 * kBM + sub * 32);
         }
         ++pq;
-        pc += 2;
+        pc += kParts;
       }
     };
     prefetch_upto(kResAhead - 1);
@@ -484,15 +497,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulators are in registers, so their latency hides behind chunk c's math.
       uint32_t r[32];
       uint4 bq[4];
-      if (half < nch) {
-        tmem_ld32(tbase + 32 * half, r);
-        load_bias(p, n0 + 32 * half, bq);
+      if (part < nch) {
+        tmem_ld32(tbase + 32 * part, r);
+        load_bias(p, n0 + 32 * part, bq);
       }
       // row statistics of this tile for the next LayerNorm: sums of x - x0 and of its
       // square, x0 = the row's first value in the tile (a shift that keeps the sums small)
       float st_x0 = 0.0f, st_s1 = 0.0f, st_s2 = 0.0f, st_s1b = 0.0f, st_s2b = 0.0f;
 #pragma unroll 1
-      for (int c = half; c < nch; c += 2, ++q) {
+      for (int c = part; c < nch; c += kParts, ++q) {
         const int kb = q % C::kEpiRing;
         uint8_t* blk = ring + kb * C::kEpiBlock;
         prefetch_upto(q + kResAhead);
@@ -510,9 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    __uint_as_float(r[8 * g + 2 * i + 1]), row_scale, row_scale, t.x, t.y);
           }
         }
-        if (c + 2 < nch) {
-          tmem_ld32(tbase + 32 * (c + 2), r);
-          load_bias(p, n + 64, bq);
+        if (c + kParts < nch) {
+          tmem_ld32(tbase + 32 * (c + kParts), r);
+          load_bias(p, n + 32 * kParts, bq);
         }
         if (p.pos) {
           const size_t poff = size_t(row % p.pos_rows) * size_t(p.N) + size_t(n);
@@ -542,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();  // every lane has read its residual row before the block is overwritten
         }
-        if (p.ln_part) {  // two-lane sums: (even, odd) columns
-          if (c == half) st_x0 = v[0];
+        if (kParts == 2 && p.ln_part) {  // two-lane sums: (even, odd) columns
+          if (c == part) st_x0 = v[0];
 #pragma unroll
           for (int g = 0; g < 4; ++g)
             if (g < ngroups) {
@@ -630,12 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_commit();
         }
       }
-      if (p.ln_part && ok && row < p.M && half < nch) {  // (mean, M2) of this row's columns of the tile
+      // (mean, M2) of this row's columns of the tile, one entry per warp of the quarter
+      // (two: the statistics are written by the F16 kernels only)
+      if (kParts == 2 && p.ln_part && ok && row < p.M && part < nch) {
         const int w = min(BN, p.N - n0);
         int cols = 0;  // this warp's columns of the tile
-        for (int c = half; c < nch; c += 2) cols += min(32, w - 32 * c);
+        for (int c = part; c < nch; c += kParts) cols += min(32, w - 32 * c);
         const float s1 = st_s1 + st_s1b, m1 = s1 / float(cols);
-        p.ln_part[(size_t(row) * p.n_tiles + nt) * 2 + half] =
+        p.ln_part[(size_t(row) * p.n_tiles + nt) * 2 + part] =
             make_float2(st_x0 + m1, fmaxf(st_s2 + st_s2b - s1 * m1, 0.0f));
       }
       tc_fence_before();
@@ -665,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, bool FP8, bool PAIR, int ATOMS = 1>
 sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
-  using C = Cfg<BN, PAIR, ATOMS>;
+  using C = Cfg<BN, PAIR, ATOMS, epi_warps<FP8, PAIR>()>;
   auto kern = gemm_tc_kernel<BN, FP8, PAIR, ATOMS>;
   // the attribute is per device: set it once on each device the kernel runs on
   static unsigned long long attr_set = 0;
@@ -684,7 +699,7 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(unsigned(PAIR ? 2 * units : units), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(gemm_threads<FP8, PAIR>(), 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
   // programmatic stream serialization: the prologue (barriers, TMEM, tensor-map
@@ -806,9 +821,10 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
   g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && (K >= 1024 || N >= 2048);
   g->bn = gemm_pick_bn(M, N, K, g->mc);
   if (g->mc && g->bn > kPairMaxBn) g->bn = kPairMaxBn;
-  // two swizzle rows of K per stage for 256-wide CTA-pair tiles over a short K that they
-  // divide (see Cfg; E4M3 over K = 1152 would leave half of its last stage empty)
-  g->atoms = (g->mc && g->bn == 256 && K <= 2048 && K % (2 * (fp8 ? kSwzBytes : kSwzBytes / 2)) == 0) ? 2 : 1;
+  // two swizzle rows of K per stage for 256-wide F16 CTA-pair tiles over a short K that
+  // they divide (see Cfg). Not for E4M3: over K = 1152 half of the last stage would be
+  // empty, and with the E4M3 pairs' wider epilogue only two 64 KB stages would fit.
+  g->atoms = (!fp8 && g->mc && g->bn == 256 && K <= 2048 && K % (2 * kSwzBytes / 2) == 0) ? 2 : 1;
   // A narrower last column tile (N % bn columns) runs MMAs of its own width, rounded
   // up to 16 columns (32 for a CTA pair, whose CTAs hold half of the W rows each).
   const int rem = N % g->bn;
@@ -914,8 +930,9 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.blk_col0 = e.blk_col0;
   p.blk_qk8 = e.blk_qk8;
   p.ln_part = e.ln_part;
-  if (e.ln_part && (e.blk_out || 2 * p.n_tiles > kMaxLnTiles)) {
-    set_error("gemm: row statistics need a row-major output of at most %d column tiles", kMaxLnTiles / 2);
+  if (e.ln_part && (e.blk_out || 2 * p.n_tiles > kMaxLnTiles || (g.fp8 && g.mc))) {
+    set_error("gemm: row statistics need a row-major output of at most %d column tiles (and not E4M3 operands "
+              "with CTA pairs)", kMaxLnTiles / 2);
     return SV_ERR_INVALID_ARG;
   }
   p.blk_tiles = (e.blk_T + 127) / 128;
@@ -936,7 +953,6 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
     case 258: return launch_bn<256, false, true>(g, p, s);
     case 259: return launch_bn<256, true, true>(g, p, s);
     case 262: return launch_bn<256, false, true, 2>(g, p, s);
-    case 263: return launch_bn<256, true, true, 2>(g, p, s);
     case 192: return launch_bn<192, false, false>(g, p, s);
     case 193: return launch_bn<192, true, false>(g, p, s);
     case 194: return launch_bn<192, false, true>(g, p, s);
