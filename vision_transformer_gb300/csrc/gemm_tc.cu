@@ -88,7 +88,9 @@ struct Cfg {
   static constexpr int kEpiBlock = 2048;
   static constexpr int kEpiRing = 2;
   static constexpr int kEpiBytes = EPI * kEpiRing * kEpiBlock;
-  static constexpr int kBarBytes = 384;
+  // barriers (full / empty per stage, at most 8 stages; 2 + 2 accumulator; drain; per
+  // epilogue warp and ring block) and the TMEM address slot
+  static constexpr int kBarBytes = (8 * (2 * 8 + 5 + EPI * kEpiRing) + 8 + 63) / 64 * 64;
   static constexpr int kBudget = 232448 - 1024 - kEpiBytes - kBarBytes;
   static constexpr int kStages = kBudget / kStage < 8 ? kBudget / kStage : 8;
   static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
@@ -205,6 +207,10 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
                    const Params p) {
   constexpr int kEpiWarps = epi_warps<FP8, PAIR>();
   constexpr int kParts = kEpiWarps / 4;  // epilogue warps per TMEM lane quarter
+  // With two warps per quarter the TMEM load of a warp's next chunk is issued during
+  // this chunk's math. With three (128 registers a thread) each chunk loads its own:
+  // measured on the E4M3 encoder, 3.5% faster per step at batch 32 than loading ahead.
+  constexpr bool kLdAhead = kParts < 3;
   using C = Cfg<BN, PAIR, ATOMS, kEpiWarps>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
       uint32_t r[32];
       uint4 bq[4];
       if (part < nch) {
-        tmem_ld32(tbase + 32 * part, r);
+        if (kLdAhead) tmem_ld32(tbase + 32 * part, r);
         load_bias(p, n0 + 32 * part, bq);
       }
       // row statistics of this tile for the next LayerNorm: sums of x - x0 and of its
@@ -511,6 +517,7 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
         prefetch_upto(q + kResAhead);
         const int n = n0 + 32 * c;
         const int ngroups = min(4, (p.N - n) / 8);  // groups of 8 columns below N
+        if (!kLdAhead) tmem_ld32(tbase + 32 * c, r);
         tmem_ld_wait(r);
         float v[32];
 #pragma unroll
@@ -524,7 +531,7 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
           }
         }
         if (c + kParts < nch) {
-          tmem_ld32(tbase + 32 * (c + kParts), r);
+          if (kLdAhead) tmem_ld32(tbase + 32 * (c + kParts), r);
           load_bias(p, n + 32 * kParts, bq);
         }
         if (p.pos) {
