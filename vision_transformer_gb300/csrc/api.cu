@@ -128,6 +128,8 @@ struct Plan {
   __half* QKV = nullptr;  // head-blocked Q/K/V for attention; the MAP KV projection reuses it row-major
   void* O = nullptr;      // [M, D] attention output (GEMM operand)
   void* Hh = nullptr;     // [M, F] GELU output (GEMM operand)
+  float* ws = nullptr;    // partial sums of the GEMMs that split K (small batches)
+  size_t ws_bytes = 0;
   GemmCall patch;
   std::vector<GemmCall> qkv, out, fc1, fc2;
   MapPlan map;
@@ -138,6 +140,8 @@ void* g_attn_scratch = nullptr;  // head-blocked copy of sv_attention's input
 size_t g_attn_scratch_bytes = 0;
 void* g_lng_scratch = nullptr;  // sv_ln_gemm: scaled weights, column sums, biases, row statistics
 size_t g_lng_scratch_bytes = 0;
+void* g_gemm_ws = nullptr;  // sv_gemm_bias_act: partial sums of a GEMM that splits K
+size_t g_gemm_ws_bytes = 0;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Step graphs of sv_encode: one per (pixels, out, batch, layers, dtype, flags) seen at
@@ -176,6 +180,9 @@ void free_plans() {
   if (g_lng_scratch) cudaFree(g_lng_scratch);
   g_lng_scratch = nullptr;
   g_lng_scratch_bytes = 0;
+  if (g_gemm_ws) cudaFree(g_gemm_ws);
+  g_gemm_ws = nullptr;
+  g_gemm_ws_bytes = 0;
 }
 
 void free_weights() {
@@ -349,12 +356,30 @@ struct Carver {
   }
 };
 
+// K ranges a small-M, long-K GEMM may be split into (given a partial-sum workspace).
+constexpr int kMaxSplits = 8;
+
+// A GEMM call; with a workspace `ws` of `ws_bytes` that holds its partial sums, the GEMM
+// may split K.
 sv_status make_call(GemmCall* c, const void* A, const void* W, int M, int N, int K, int fp8, const GemmEpi& e,
-                    int k_logical) {
+                    int k_logical, float* ws = nullptr, size_t ws_bytes = 0) {
   c->e = e;
   c->k = k_logical;
-  SV_TRY(gemm_prepare(&c->g, A, W, M, N, K, fp8));
+  const int splits = (ws && gemm_splitk_ws_bytes_for(M, N, K, fp8, kMaxSplits) <= ws_bytes) ? kMaxSplits : 1;
+  SV_TRY(gemm_prepare(&c->g, A, W, M, N, K, fp8, true, splits));
+  if (c->g.k_splits > 1) c->e.ws = ws;
   return gemm_bind_epilogue(&c->g, c->e);
+}
+
+// Largest split-K workspace over the MAP head's GEMMs for B images.
+size_t map_ws_bytes(int B, int fp8) {
+  const Dims& d = g_w.d;
+  const size_t a = gemm_splitk_ws_bytes_for(1, d.D, d.D, fp8, kMaxSplits);
+  const size_t b = gemm_splitk_ws_bytes_for(B * d.T, 2 * d.D, d.D, fp8, kMaxSplits);
+  const size_t c = gemm_splitk_ws_bytes_for(B, d.D, d.D, fp8, kMaxSplits);
+  const size_t e = gemm_splitk_ws_bytes_for(B, d.F, d.D, fp8, kMaxSplits);
+  const size_t f = gemm_splitk_ws_bytes_for(B, d.D, d.F, fp8, kMaxSplits);
+  return std::max(std::max(std::max(a, b), std::max(c, e)), f);
 }
 
 GemmEpi epi(const __half* bias, void* out, float scale, int act = SV_ACT_NONE, int out_e4m3 = 0,
@@ -371,7 +396,8 @@ GemmEpi epi(const __half* bias, void* out, float scale, int act = SV_ACT_NONE, i
 
 // Buffers of the MAP head (carved from `c`); xf is the encoder-output operand.
 // The final projection's output is the caller's buffer: it is bound per call.
-sv_status build_map(MapPlan& m, Carver& c, const void* xf, int B, int fp8, bool carve_kv, __half* kv_alias) {
+sv_status build_map(MapPlan& m, Carver& c, const void* xf, int B, int fp8, bool carve_kv, __half* kv_alias,
+                    float* ws, size_t ws_bytes) {
   const Dims& d = g_w.d;
   const size_t eb = fp8 ? 1 : 2;
   m.qv = static_cast<__half*>(c.take(size_t(d.D) * 2));
@@ -384,15 +410,20 @@ sv_status build_map(MapPlan& m, Carver& c, const void* xf, int B, int fp8, bool 
   const float sc = fp8 ? 1.0f / 256.0f : 1.0f;
   const int D = d.D, F = d.F;
   SV_TRY(make_call(&m.q, fp8 ? (const void*)g_w.probe8 : g_w.probe, fp8 ? (const void*)g_w.mq_w8 : g_w.mq_w, 1, D, D,
-                   fp8, epi(g_w.mq_b, m.qv, sc), D));
+                   fp8, epi(g_w.mq_b, m.qv, sc), D, ws, ws_bytes));
   SV_TRY(make_call(&m.kv, xf, fp8 ? (const void*)g_w.mkv_w8 : g_w.mkv_w, B * d.T, 2 * D, D, fp8,
-                   epi(g_w.mkv_b, m.KV, sc), D));
-  SV_TRY(make_call(&m.out, m.a, fp8 ? (const void*)g_w.mo_w8 : g_w.mo_w, B, D, D, fp8, epi(g_w.mo_b, m.A, sc), D));
+                   epi(g_w.mkv_b, m.KV, sc), D, ws, ws_bytes));
+  SV_TRY(make_call(&m.out, m.a, fp8 ? (const void*)g_w.mo_w8 : g_w.mo_w, B, D, D, fp8, epi(g_w.mo_b, m.A, sc), D, ws,
+                   ws_bytes));
   SV_TRY(make_call(&m.fc1, m.Ya, fp8 ? (const void*)g_w.mfc1_w8 : g_w.mfc1_w, B, F, D, fp8,
-                   epi(g_w.mfc1_b, m.Ha, sc, SV_ACT_GELU_TANH, fp8), D));
+                   epi(g_w.mfc1_b, m.Ha, sc, SV_ACT_GELU_TANH, fp8), D, ws, ws_bytes));
+  // the final projection's output is bound per call (run_map)
   m.fc2.e = epi(g_w.mfc2_b, nullptr, sc, SV_ACT_NONE, 0, m.A);
   m.fc2.k = F;
-  return gemm_prepare(&m.fc2.g, m.Ha, fp8 ? (const void*)g_w.mfc2_w8 : g_w.mfc2_w, B, D, F, fp8);
+  const int splits = (ws && gemm_splitk_ws_bytes_for(B, D, F, fp8, kMaxSplits) <= ws_bytes) ? kMaxSplits : 1;
+  SV_TRY(gemm_prepare(&m.fc2.g, m.Ha, fp8 ? (const void*)g_w.mfc2_w8 : g_w.mfc2_w, B, D, F, fp8, true, splits));
+  if (m.fc2.g.k_splits > 1) m.fc2.e.ws = ws;
+  return SV_OK;
 }
 
 sv_status alloc_carved(Carver& c, void** mem, size_t* bytes) {
@@ -425,8 +456,17 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
   p->qkv_calls = (flags & SV_ENCODE_UNFUSED_QKV) ? 3 : 1;
   p->qk8 = (flags & SV_ENCODE_FP8_ATTENTION) ? 1 : 0;
   p->fold_ln = !fp8;
+  // split-K partial sums: the largest need over the plan's GEMMs (0 at large batches)
+  {
+    const int Mi = int(M), wq = 3 * d.D / p->qkv_calls;
+    size_t need = map_ws_bytes(B, fp8);
+    const int shapes[5][3] = {{Mi, d.D, d.Kp}, {Mi, wq, d.D}, {Mi, d.D, d.D}, {Mi, d.F, d.D}, {Mi, d.D, d.F}};
+    for (const auto& sh : shapes) need = std::max(need, gemm_splitk_ws_bytes_for(sh[0], sh[1], sh[2], fp8, kMaxSplits));
+    p->ws_bytes = need;
+  }
   Carver c{nullptr};
   for (int pass = 0; pass < 2; ++pass) {
+    p->ws = p->ws_bytes ? static_cast<float*>(c.take(p->ws_bytes)) : nullptr;
     p->A0 = c.take(M * d.Kp * eb);
     p->X = static_cast<__half*>(c.take(M * d.D * 2));
     p->Y = c.take(M * d.D * eb);
@@ -437,7 +477,7 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
     p->QKV = static_cast<__half*>(c.take(qkv_bytes > M * 3 * d.D * 2 ? qkv_bytes : M * 3 * d.D * 2));
     p->O = c.take(M * d.D * eb);
     p->Hh = c.take(M * d.F * eb);
-    SV_TRY(build_map(p->map, c, p->Y, B, fp8, false, p->QKV));
+    SV_TRY(build_map(p->map, c, p->Y, B, fp8, false, p->QKV, p->ws, p->ws_bytes));
     if (pass == 0) {
       sv_status st = alloc_carved(c, &p->mem, &p->bytes);
       if (st != SV_OK) return st;
@@ -455,7 +495,8 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
   pe.pos_rows = d.T;
   // F16: the GEMMs that write X also write its row statistics for the next LayerNorm
   if (p->fold_ln) pe.ln_part = p->ln_part;
-  if ((st = make_call(&p->patch, p->A0, fp8 ? (const void*)g_w.patch_w8 : g_w.patch_w, Mi, d.D, d.Kp, fp8, pe, d.P)))
+  if ((st = make_call(&p->patch, p->A0, fp8 ? (const void*)g_w.patch_w8 : g_w.patch_w, Mi, d.D, d.Kp, fp8, pe, d.P,
+                      p->ws, p->ws_bytes)))
     return fail(st);
   p->qkv.resize(size_t(d.L) * size_t(p->qkv_calls));
   p->out.resize(size_t(d.L));
@@ -491,15 +532,18 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
       qe.blk_col0 = int(r0);
       qe.blk_qk8 = p->qk8;
       const void* wptr = fp8 ? static_cast<const void*>(w.qkv_w8 + r0 * d.D) : static_cast<const void*>(w.qkv_w + r0 * d.D);
-      st = make_call(&p->qkv[i * size_t(nq) + size_t(j)], ln_in, wptr, Mi, wq, d.D, fp8, qe, d.D);
+      st = make_call(&p->qkv[i * size_t(nq) + size_t(j)], ln_in, wptr, Mi, wq, d.D, fp8, qe, d.D, p->ws, p->ws_bytes);
     }
     GemmEpi oe = epi(w.out_b, p->X, sc, SV_ACT_NONE, 0, p->X);
     GemmEpi de = epi(w.fc2_b, p->X, sc, SV_ACT_NONE, 0, p->X);
     if (p->fold_ln) oe.ln_part = de.ln_part = p->ln_part;
     if (st ||
-        (st = make_call(&p->out[i], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8, oe, d.D)) ||
-        (st = make_call(&p->fc1[i], ln_in, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8, fe, d.D)) ||
-        (st = make_call(&p->fc2[i], p->Hh, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, Mi, d.D, d.F, fp8, de, d.F)))
+        (st = make_call(&p->out[i], p->O, fp8 ? (const void*)w.out_w8 : w.out_w, Mi, d.D, d.D, fp8, oe, d.D, p->ws,
+                        p->ws_bytes)) ||
+        (st = make_call(&p->fc1[i], ln_in, fp8 ? (const void*)w.fc1_w8 : w.fc1_w, Mi, d.F, d.D, fp8, fe, d.D, p->ws,
+                        p->ws_bytes)) ||
+        (st = make_call(&p->fc2[i], p->Hh, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, Mi, d.D, d.F, fp8, de, d.F, p->ws,
+                        p->ws_bytes)))
       return fail(st);
   }
   *out = p.get();
@@ -517,6 +561,16 @@ double gemm_bytes(const GemmOperands& g, const GemmEpi& e, int k_logical) {
 }
 
 sv_status run_gemm(const GemmCall& c, cudaStream_t s) {
+  if (c.g.k_splits > 1) {  // two launches: the K ranges' partial sums, then their reduction and the epilogue
+    const double ws = double(gemm_splitk_ws_bytes(c.g));
+    const double eb = c.g.fp8 ? 1.0 : 2.0;
+    {
+      Launch L(kKindGemm, gemm_flops(c.g, c.k), (double(c.g.M) + double(c.g.N)) * c.k * eb + ws, s);
+      SV_TRY(gemm_launch(c.g, c.e, s, 0));
+    }
+    Launch L(kKindGemm, 0.0, ws + gemm_bytes(c.g, c.e, 0), s);
+    return gemm_launch(c.g, c.e, s, 1);
+  }
   Launch L(kKindGemm, gemm_flops(c.g, c.k), gemm_bytes(c.g, c.e, c.k), s);
   return gemm_launch(c.g, c.e, s);
 }
@@ -913,8 +967,26 @@ sv_status sv_gemm_bias_act(const void* A, const void* W, const void* bias, const
   GemmEpi e = epi(static_cast<const __half*>(bias), C, scale, act, out_dtype, static_cast<const __half*>(residual));
   e.pos = static_cast<const __half*>(pos);
   e.pos_rows = pos_rows;
+  // a small-M, long-K GEMM splits K: its partial sums go to a library buffer that grows
+  // to the largest need seen (freed by sv_shutdown)
+  const size_t need = gemm_splitk_ws_bytes_for(M, N, K, in_dtype, kMaxSplits);
+  if (need > g_gemm_ws_bytes) {
+    if (g_gemm_ws) {
+      SV_CHECK_CUDA(cudaDeviceSynchronize(), "sv_gemm_bias_act");
+      cudaFree(g_gemm_ws);
+      g_gemm_ws = nullptr;
+      g_gemm_ws_bytes = 0;
+    }
+    cudaError_t ce = cudaMalloc(&g_gemm_ws, need);
+    if (ce != cudaSuccess) {
+      cudaGetLastError();
+      set_error("sv_gemm_bias_act: cudaMalloc of %zu bytes for the split-K partial sums failed", need);
+      return SV_ERR_OOM;
+    }
+    g_gemm_ws_bytes = need;
+  }
   GemmCall c;
-  SV_TRY(make_call(&c, A, W, M, N, K, in_dtype, e, K));
+  SV_TRY(make_call(&c, A, W, M, N, K, in_dtype, e, K, static_cast<float*>(g_gemm_ws), g_gemm_ws_bytes));
   return run_gemm(c, static_cast<cudaStream_t>(stream));
 }
 
@@ -1138,10 +1210,12 @@ sv_status sv_map_pool(const void* x, void* out, int batch, int gemm_dtype, void*
     np->B = batch;
     np->fp8 = fp8;
     Carver c{nullptr};
+    np->ws_bytes = map_ws_bytes(batch, fp8);
     for (int pass = 0; pass < 2; ++pass) {
+      np->ws = np->ws_bytes ? static_cast<float*>(c.take(np->ws_bytes)) : nullptr;
       np->Y = fp8 ? c.take(size_t(batch) * d.T * d.D) : nullptr;  // quantised copy of x
       if (c.base && !fp8) np->Y = const_cast<void*>(x);
-      SV_TRY(build_map(np->map, c, np->Y ? np->Y : x, batch, fp8, true, nullptr));
+      SV_TRY(build_map(np->map, c, np->Y ? np->Y : x, batch, fp8, true, nullptr, np->ws, np->ws_bytes));
       if (pass == 0) SV_TRY(alloc_carved(c, &np->mem, &np->bytes));
     }
     p = np.get();

@@ -336,15 +336,6 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, int* err) {
 // var = M2 / width (biased, as the LayerNorm kernel) and the same r / aug outputs as its
 // statistics mode.
 
-// (n, mean, m2) <- merge with (nb, mb, m2b); a side with no columns leaves the other.
-__device__ __forceinline__ void chan_merge(float& n, float& mean, float& m2, float nb, float mb, float m2b) {
-  if (nb == 0.0f) return;
-  const float nn = n + nb, d = mb - mean, f = __fdividef(nb, nn);
-  mean = fmaf(d, f, mean);
-  m2 += m2b + d * d * (n * f);
-  n = nn;
-}
-
 template <int kLanes>
 __global__ void __launch_bounds__(128) ln_finalize_kernel(const float2* __restrict__ part, int tiles, int tile_w,
                                                          float* __restrict__ r, __half* __restrict__ aug,

@@ -25,6 +25,9 @@
 //               TMA store; residual blocks arrive by TMA one chunk ahead; the
 //               GEMMs that write the residual stream also leave per-tile row
 //               statistics for the next LayerNorm.
+// Split K (small M, long K: tiles that would fill few SMs): the work items are
+// (tile, K range) pairs; each writes its raw F32 sums to a workspace and
+// gemm_splitk_reduce_kernel adds them up in a fixed order and applies the epilogue.
 // Launched with programmatic stream serialization: the prologue overlaps the
 // previous kernel, global memory is touched only after griddepcontrol.wait.
 // F16 operands use kind::f16 (K = 16 per instruction); E4M3 operands use
@@ -123,6 +126,11 @@ struct Params {
   int blk_col0;  // first column of the fused [Q | K | V] space this GEMM's columns start at
   int blk_qk8;   // Q and K as E4M3 (16 x value): 16-byte groups of 16 columns per row
   float2* ln_part;  // per (row, column tile): (mean, M2) of the results, or null
+  // split K: item = tile * k_splits + split; split s runs the K blocks
+  // [s kb_split, min(k_blocks, (s + 1) kb_split)) and stores its raw sums in rows
+  // s * ws_m_tiles * 128 + (tile row) of the row-major F32 workspace (through tmC)
+  int k_splits, kb_split;
+  int ws_m_tiles;
 };
 
 // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), with
@@ -198,7 +206,8 @@ __device__ __forceinline__ void tile_of(const Params& p, int it, int rank, int& 
   mt = PAIR ? 2 * mu + rank : mu;
 }
 
-template <int BN, bool FP8, bool PAIR, int ATOMS>
+// SPLIT: items are (tile, K range) pairs whose raw sums go to the split-K workspace.
+template <int BN, bool FP8, bool PAIR, int ATOMS, bool SPLIT>
 __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmWt, const __grid_constant__ CUtensorMap tmC,
@@ -233,7 +242,18 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
   const bool leader = rank == 0;
   const int it0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
   const int it_step = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
-  const int num_items = PAIR ? ((p.m_tiles + 1) / 2) * p.n_tiles : p.m_tiles * p.n_tiles;
+  const int k_splits = SPLIT ? p.k_splits : 1;
+  const int num_items = (PAIR ? ((p.m_tiles + 1) / 2) * p.n_tiles : p.m_tiles * p.n_tiles) * k_splits;
+  // K blocks of item it: [kb_lo, kb_hi)
+  auto k_range = [&](int it, int& kb_lo, int& kb_hi) {
+    if (SPLIT) {
+      kb_lo = (it % k_splits) * p.kb_split;
+      kb_hi = min(p.k_blocks, kb_lo + p.kb_split);
+    } else {
+      kb_lo = 0;
+      kb_hi = p.k_blocks;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -279,9 +299,10 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
       uint32_t issued = 0, issued_phase = 0;  // stages with loads in flight, and their phase bit
       bool ok = true;
       for (int it = it0; it < num_items && ok; it += it_step) {
-        int mt, nt;
-        tile_of<PAIR>(p, it, rank, mt, nt);
-        for (int kb = 0; kb < p.k_blocks + aug_blocks; ++kb) {
+        int mt, nt, kb_lo, kb_hi;
+        tile_of<PAIR>(p, it / k_splits, rank, mt, nt);
+        k_range(it, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi + aug_blocks; ++kb) {
           if (!mbar_wait<kSleepProducer>(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.err)) {
             ok = false;
             break;
@@ -366,13 +387,14 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
       for (int it = it0; it < num_items && ok; it += it_step, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        int mt_i, nt_i;
-        tile_of<PAIR>(p, it, rank, mt_i, nt_i);
+        int mt_i, nt_i, kb_lo, kb_hi;
+        tile_of<PAIR>(p, it / k_splits, rank, mt_i, nt_i);
+        k_range(it, kb_lo, kb_hi);
         const uint32_t idesc = (nt_i == p.n_full && p.tail_n) ? idesc_tail : idesc_full;
         if (!mbar_wait<kSleepMma>(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(acc * BN);
-        for (int kb = 0; kb < p.k_blocks + aug_blocks; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi + aug_blocks; ++kb) {
           if (!mbar_wait<kSleepMma>(bar_full + 8 * stage, phase, abort_flag, p.err)) {
             ok = false;
             break;
@@ -391,7 +413,7 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
           for (int j = 0; j < 4 * ATOMS; ++j) {  // 4 instructions x 32 bytes of K per swizzle row
             const uint64_t ad = make_sdesc(sa + (j >> 2) * C::kAtomA + 32 * (j & 3), 16, 1024, 2);
             const uint64_t bd = make_sdesc(sb + (j >> 2) * C::kAtomB + 32 * (j & 3), 16, 1024, 2);
-            const uint32_t accum = (kb | j) != 0;
+            const uint32_t accum = ((kb - kb_lo) | j) != 0;
             if (PAIR) {
               if (FP8)
                 mma_f8_pair(d, ad, bd, idesc, accum);
@@ -458,7 +480,7 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
     auto prefetch_upto = [&](int qmax) {  // issue residual loads for chunks pq .. qmax
       while (p.has_res && pq <= qmax && pit < num_items) {
         int mt2, nt2;
-        tile_of<PAIR>(p, pit, rank, mt2, nt2);
+        tile_of<PAIR>(p, pit / k_splits, rank, mt2, nt2);
         if (pc >= tile_chunks(p, nt2, BN)) {  // no (more) chunks of this warp in the tile
           pc = part;
           pit += it_step;
@@ -485,7 +507,7 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
     const uint32_t tempty_lead0 = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
     for (int it = it0; it < num_items && ok; it += it_step, ++local) {
       int mt, nt;
-      tile_of<PAIR>(p, it, rank, mt, nt);
+      tile_of<PAIR>(p, it / k_splits, rank, mt, nt);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const int row0 = mt * kBM + sub * 32;
@@ -499,6 +521,33 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
       if (!__all_sync(0xffffffffu, mbar_wait<kSleepEpi>(bar_tfull + 8 * acc, acc_phase, abort_flag, p.err))) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + uint32_t(acc * BN) + (uint32_t(sub * 32) << 16);
+      if (SPLIT) {  // this K range's raw sums: each 32 x 32 F32 chunk staged in the warp's
+                    // 4 KB (128-byte swizzle) and written by one TMA store to the workspace
+        const int wrow = ((it % k_splits) * p.ws_m_tiles + mt) * kBM + sub * 32;
+        for (int c = part; c < nch; c += kParts) {
+          if (lane == 0) bulk_wait_read<0>();  // the previous chunk's store has read the block
+          __syncwarp();
+          uint32_t pr[32];
+          tmem_ld32(tbase + 32 * c, pr);
+          tmem_ld_wait(pr);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(ring + lane * 128 + 16 * (u ^ (lane & 7))) =
+                make_uint4(pr[4 * u], pr[4 * u + 1], pr[4 * u + 2], pr[4 * u + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, smem_u32(ring), nt * BN + 32 * c, wrow);
+            bulk_commit();
+          }
+        }
+        tc_fence_before();
+        if (PAIR)
+          mbar_arrive_cluster(tempty_lead0 + 8 * acc);
+        else
+          mbar_arrive(bar_tempty + 8 * acc);
+        continue;
+      }
       // The TMEM load and the bias of chunk c + 1 are issued as soon as chunk c's
       // accumulators are in registers, so their latency hides behind chunk c's math.
       uint32_t r[32];
@@ -685,10 +734,116 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
   }
 }
 
-template <int BN, bool FP8, bool PAIR, int ATOMS = 1>
+// Split-K reduction and epilogue. One warp per (row, 256-column tile), eight
+// consecutive columns per lane (lane / 4 = the 32-column chunk): the splits' partial
+// sums are added in split order (the result does not depend on the schedule), then
+// scale, bias, positions, tanh-GELU, residual and the F16 / E4M3 store as in the GEMM
+// epilogue, and the same per-half row statistics (chunks h, h + 2, ... of the tile,
+// merged across lanes) for the next LayerNorm.
+struct ReduceParams {
+  const float* ws;
+  int k_splits, m_pad, n_pad, n_tiles;  // workspace: k_splits x [m_pad, n_pad] F32, 256-wide tiles
+  int M, N;
+  float scale;
+  const __half* bias;
+  const __half* pos;
+  int pos_rows;
+  const __half* res;
+  int act, out_e4m3;
+  void* out;
+  float2* ln_part;
+};
+
+__global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const ReduceParams q) {
+  pdl_launch_dependents();
+  pdl_wait();  // the partial sums come from the GEMM launched just before
+  const int lane = threadIdx.x & 31;
+  const long wid = (long(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (wid >= long(q.M) * q.n_tiles) return;  // whole warps
+  const int row = int(wid / q.n_tiles), nt = int(wid - long(row) * q.n_tiles);
+  const int col = nt * 256 + 8 * lane;
+  const bool live = col < q.N;  // N is a multiple of 16: all eight columns exist
+  float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+  if (live) {
+    float4 a[2 * 8];
+    const int ns = q.k_splits < 8 ? q.k_splits : 8;
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < ns) {
+        const float4* src = reinterpret_cast<const float4*>(q.ws + (size_t(s) * q.m_pad + row) * q.n_pad + col);
+        a[2 * s] = __ldg(src);
+        a[2 * s + 1] = __ldg(src + 1);
+      }
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < ns) {
+        v[0] += a[2 * s].x, v[1] += a[2 * s].y, v[2] += a[2 * s].z, v[3] += a[2 * s].w;
+        v[4] += a[2 * s + 1].x, v[5] += a[2 * s + 1].y, v[6] += a[2 * s + 1].z, v[7] += a[2 * s + 1].w;
+      }
+    for (int s = 8; s < q.k_splits; ++s) {
+      const float4* src = reinterpret_cast<const float4*>(q.ws + (size_t(s) * q.m_pad + row) * q.n_pad + col);
+      const float4 x = __ldg(src), y = __ldg(src + 1);
+      v[0] += x.x, v[1] += x.y, v[2] += x.z, v[3] += x.w, v[4] += y.x, v[5] += y.y, v[6] += y.z, v[7] += y.w;
+    }
+    float b[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    if (q.bias) load8h(q.bias + col, b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = fmaf(v[i], q.scale, b[i]);
+    if (q.pos) {
+      float pp[8];
+      load8h(q.pos + size_t(row % q.pos_rows) * size_t(q.N) + size_t(col), pp);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += pp[i];
+    }
+    if (q.act == SV_ACT_GELU_TANH) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) gelu_tanh_x2(v[2 * i], v[2 * i + 1]);
+    }
+    const size_t off = size_t(row) * q.N + col;
+    if (q.res) add8h(__ldg(reinterpret_cast<const uint4*>(q.res + off)), v);
+    if (!q.out_e4m3) {
+      uint4 w;
+      __half2* h = reinterpret_cast<__half2*>(&w);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+      *reinterpret_cast<uint4*>(static_cast<__half*>(q.out) + off) = w;
+    } else {
+      uint2 w;
+      __nv_fp8x2_storage_t* c8 = reinterpret_cast<__nv_fp8x2_storage_t*>(&w);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        c8[i] = __nv_cvt_float2_to_fp8x2(make_float2(16.0f * v[2 * i], 16.0f * v[2 * i + 1]), __NV_SATFINITE,
+                                         __NV_E4M3);
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(q.out) + off) = w;
+    }
+  }
+  if (q.ln_part) {  // (mean, M2): this lane's columns, its chunk, then the chunks of each parity
+    float n = 0.0f, mean = 0.0f, m2 = 0.0f;
+    if (live) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += v[i];
+      mean = sum * 0.125f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m2 = fmaf(v[i] - mean, v[i] - mean, m2);
+      n = 8.0f;
+    }
+#pragma unroll
+    for (int o = 1; o <= 16; o <<= 1) {
+      if (o == 4) continue;  // lane bit 2 is the chunk's parity: the two halves stay apart
+      const float nb = __shfl_xor_sync(0xffffffffu, n, o), mb = __shfl_xor_sync(0xffffffffu, mean, o),
+                  m2b = __shfl_xor_sync(0xffffffffu, m2, o);
+      chan_merge(n, mean, m2, nb, mb, m2b);
+    }
+    if ((lane == 0 || lane == 4) && n > 0.0f)
+      q.ln_part[(size_t(row) * q.n_tiles + nt) * 2 + (lane >> 2)] = make_float2(mean, m2);
+  }
+}
+
+template <int BN, bool FP8, bool PAIR, int ATOMS = 1, bool SPLIT = false>
 sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
   using C = Cfg<BN, PAIR, ATOMS, epi_warps<FP8, PAIR>()>;
-  auto kern = gemm_tc_kernel<BN, FP8, PAIR, ATOMS>;
+  auto kern = gemm_tc_kernel<BN, FP8, PAIR, ATOMS, SPLIT>;
   // the attribute is per device: set it once on each device the kernel runs on
   static unsigned long long attr_set = 0;
   int dev = 0;
@@ -700,7 +855,7 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm)");
     attr_set |= bit;
   }
-  const int items = PAIR ? ((prm.m_tiles + 1) / 2) * prm.n_tiles : prm.m_tiles * prm.n_tiles;
+  const int items = (PAIR ? ((prm.m_tiles + 1) / 2) * prm.n_tiles : prm.m_tiles * prm.n_tiles) * (SPLIT ? prm.k_splits : 1);
   const int slots = PAIR ? num_sms() / 2 : num_sms();  // one CTA (PAIR: one two-CTA cluster) per SM (pair)
   const int units = items < slots ? items : slots;
   cudaLaunchConfig_t cfg = {};
@@ -723,12 +878,13 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  const CUtensorMap& tr = g.has_res ? g.tr : g.tc;
+  const CUtensorMap& tcm = SPLIT ? g.tws : g.tc;  // split K: the workspace takes the output's place
+  const CUtensorMap& tr = g.has_res ? g.tr : tcm;
   const CUtensorMap& twt = (PAIR && g.tail_n) ? g.tw_tail : g.tw;
   const CUtensorMap& taa = prm.ln_aug ? g.ta_aug : g.ta;
   const CUtensorMap& twa = prm.ln_aug ? g.tw_aug : g.tw;
   const CUtensorMap& twat = (prm.ln_aug && PAIR && g.tail_n) ? g.tw_aug_tail : twa;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, g.ta, g.tw, twt, g.tc, tr, taa, twa, twat, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, g.ta, g.tw, twt, tcm, tr, taa, twa, twat, prm);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return SV_OK;
 }
@@ -791,7 +947,7 @@ sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int
 // ones measured on GB300 for 23,328-row GEMMs with the copies and epilogue
 // running (TFLOP/s at 256 / 192 / 128 / 64 columns: about 1780 / 1480 / 1000 /
 // 600): wide tiles win whenever there are enough of them to fill the SMs.
-int gemm_pick_bn(int M, int N, int K, bool pair) {
+int gemm_pick_bn(int M, int N, int K, bool pair, double* t_best) {
   const int cand[4] = {256, 192, 128, 64};
   const double rate[4] = {1780.0, 1480.0, 1000.0, 600.0};
   const int sms = num_sms() > 0 ? num_sms() : 148;
@@ -808,11 +964,46 @@ int gemm_pick_bn(int M, int N, int K, bool pair) {
       best = bn;
     }
   }
+  if (t_best) *t_best = best_t;
   return best;
 }
 
-sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8,
-                       bool allow_pair) {
+namespace {
+
+// Split K. At small M a long-K GEMM's tiles fill few SMs, each streaming all of K.
+// Splitting K into ranges gives 256-wide tiles on most SMs, plus a reduction kernel
+// whose cost does not shrink with the main loop. In gemm_pick_bn's time units (E4M3
+// main loops at half the F16 time) the reduction costs about 125, from measured times
+// (us per call, unsplit -> split): F16 729 x 1152 x 4304 24.0 -> 16.3 (5 ranges),
+// 1458 rows 25.3 -> 23.0 (2), 32 rows 22.5 -> 11.2 (8); E4M3 32 rows 12.9 -> 10.4 (8),
+// while E4M3 729 rows (14.1 vs 14.4 split) and 1458 rows (15.8 vs 19.6) stay whole.
+// Returns the number of K ranges (1: no split); sets *bn and *mc for the split layout.
+int pick_splits(int M, int N, int K, int fp8, bool allow_pair, int max_splits, double t_unsplit, int* bn,
+                int* mc) {
+  constexpr double kReduceCost = 125.0;
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  if (max_splits < 2 || K < 2048) return 1;
+  const int mt = (M + kBM - 1) / kBM;
+  const bool pair = allow_pair && mt >= 2 && sms >= 2;
+  const int w = 256;
+  const int items = (pair ? (mt + 1) / 2 : mt) * ((N + w - 1) / w);
+  const int slots = pair ? sms / 2 : sms;
+  const int k_blocks = (K + (fp8 ? kSwzBytes : kSwzBytes / 2) - 1) / (fp8 ? kSwzBytes : kSwzBytes / 2);
+  int splits = slots / items;
+  if (splits > max_splits) splits = max_splits;
+  const int min_blocks = fp8 ? 4 : 8;  // at least 512 K elements a range
+  if (splits > k_blocks / min_blocks) splits = k_blocks / min_blocks;
+  if (splits < 2) return 1;
+  const double f = fp8 ? 0.5 : 1.0;  // main-loop time relative to F16
+  const double t_split = f * double(w) / 1780.0 * double(K) / splits + kReduceCost;
+  if (t_split > 0.8 * f * t_unsplit) return 1;
+  *bn = w;
+  *mc = pair ? 1 : 0;
+  return splits;
+}
+
+// Tile, pairing, stage and split choices for an M x N x K GEMM (no tensor maps).
+void gemm_choose(GemmOperands* g, int M, int N, int K, int fp8, bool allow_pair, int max_splits) {
   g->M = M;
   g->N = N;
   g->K = K;
@@ -826,12 +1017,22 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
   // QKV GEMMs, and with two swizzle rows of K per stage 1% per step faster on the
   // 1152 x 1152 output projection (batch 32 and 128).
   g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && (K >= 1024 || N >= 2048);
-  g->bn = gemm_pick_bn(M, N, K, g->mc);
+  double t_unsplit = 0.0;
+  g->bn = gemm_pick_bn(M, N, K, g->mc, &t_unsplit);
   if (g->mc && g->bn > kPairMaxBn) g->bn = kPairMaxBn;
+  g->k_splits = pick_splits(M, N, K, fp8, allow_pair, max_splits, t_unsplit, &g->bn, &g->mc);
   // two swizzle rows of K per stage for 256-wide F16 CTA-pair tiles over a short K that
   // they divide (see Cfg). Not for E4M3: over K = 1152 half of the last stage would be
   // empty, and with the E4M3 pairs' wider epilogue only two 64 KB stages would fit.
-  g->atoms = (!fp8 && g->mc && g->bn == 256 && K <= 2048 && K % (2 * kSwzBytes / 2) == 0) ? 2 : 1;
+  g->atoms = (!fp8 && g->mc && g->bn == 256 && K <= 2048 && K % (2 * kSwzBytes / 2) == 0 && g->k_splits == 1) ? 2 : 1;
+  g->kb_split = 0;
+  if (g->k_splits > 1) {  // equal ranges of whole stages; no range is empty
+    const int bk = (fp8 ? kSwzBytes : kSwzBytes / 2) * g->atoms;
+    const int k_blocks = (K + bk - 1) / bk;
+    g->kb_split = (k_blocks + g->k_splits - 1) / g->k_splits;
+    g->k_splits = (k_blocks + g->kb_split - 1) / g->kb_split;
+  }
+
   // A narrower last column tile (N % bn columns) runs MMAs of its own width, rounded
   // up to 16 columns (32 for a CTA pair, whose CTAs hold half of the W rows each).
   const int rem = N % g->bn;
@@ -863,6 +1064,26 @@ sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int
     const double a_bytes = double(M) * K * (fp8 ? 1 : 2);
     if (units > 0 && a_bytes <= 64e6 && makespan(true) * 20 <= makespan(false) * 19) g->tail_last = 1;
   }
+}
+
+}  // namespace
+
+size_t gemm_splitk_ws_bytes(const GemmOperands& g) {
+  if (g.k_splits <= 1) return 0;
+  const int mt = (g.M + kBM - 1) / kBM, m_tiles = g.mc ? 2 * ((mt + 1) / 2) : mt;
+  const int n_tiles = (g.N + g.bn - 1) / g.bn;
+  return size_t(g.k_splits) * m_tiles * n_tiles * size_t(kBM) * g.bn * sizeof(float);
+}
+
+size_t gemm_splitk_ws_bytes_for(int M, int N, int K, int fp8, int max_splits) {
+  GemmOperands g;
+  gemm_choose(&g, M, N, K, fp8, true, max_splits);
+  return gemm_splitk_ws_bytes(g);
+}
+
+sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8,
+                       bool allow_pair, int max_splits) {
+  gemm_choose(g, M, N, K, fp8, allow_pair, max_splits);
   sv_status st = gemm_operand_map(&g->ta, A, M, K, fp8, kBM);
   if (st != SV_OK) return st;
   st = gemm_operand_map(&g->tw, W, N, K, fp8, g->mc ? g->bn / 2 : g->bn);
@@ -905,15 +1126,65 @@ sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e) {
   g->out = e.out;
   g->out_e4m3 = e.out_e4m3;
   g->res = e.residual;
+  g->ws = nullptr;
+  if (g->k_splits > 1 && e.ws) {  // split K: [k_splits * m_pad, n_pad] F32, 32 x 32 blocks, 128-byte swizzle
+    const int mt = (g->M + kBM - 1) / kBM, m_pad = (g->mc ? 2 * ((mt + 1) / 2) : mt) * kBM;
+    const int n_pad = (g->N + g->bn - 1) / g->bn * g->bn;
+    const uint64_t dims[2] = {uint64_t(n_pad), uint64_t(g->k_splits) * uint64_t(m_pad)};
+    const uint64_t strides[1] = {uint64_t(n_pad) * 4u};
+    const uint32_t box[2] = {32, 32};
+    st = make_tmap(&g->tws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, e.ws, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != SV_OK) return st;
+    g->ws = e.ws;
+  }
   if (g->has_res) return gemm_output_map(&g->tr, e.residual, g->M, g->N, 0);
   return SV_OK;
 }
 
-sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
+namespace {
+
+sv_status launch_main(const GemmOperands& g, const Params& p, cudaStream_t s, bool split) {
+  if (split) {  // split K: 256-wide tiles, one swizzle row of K per stage (gemm_choose)
+    const int key = (g.bn == 256 && g.atoms == 1) ? (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0) : -1;
+    switch (key) {
+      case 0: return launch_bn<256, false, false, 1, true>(g, p, s);
+      case 1: return launch_bn<256, true, false, 1, true>(g, p, s);
+      case 2: return launch_bn<256, false, true, 1, true>(g, p, s);
+      case 3: return launch_bn<256, true, true, 1, true>(g, p, s);
+      default: set_error("gemm: no split-K kernel for tile width %d", g.bn); return SV_ERR_UNSUPPORTED;
+    }
+  }
+  const int key = g.bn | (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0) | (g.atoms == 2 ? 4 : 0);
+  switch (key) {
+    case 256: return launch_bn<256, false, false>(g, p, s);
+    case 257: return launch_bn<256, true, false>(g, p, s);
+    case 258: return launch_bn<256, false, true>(g, p, s);
+    case 259: return launch_bn<256, true, true>(g, p, s);
+    case 262: return launch_bn<256, false, true, 2>(g, p, s);
+    case 192: return launch_bn<192, false, false>(g, p, s);
+    case 193: return launch_bn<192, true, false>(g, p, s);
+    case 194: return launch_bn<192, false, true>(g, p, s);
+    case 195: return launch_bn<192, true, true>(g, p, s);
+    case 128: return launch_bn<128, false, false>(g, p, s);
+    case 129: return launch_bn<128, true, false>(g, p, s);
+    case 130: return launch_bn<128, false, true>(g, p, s);
+    case 131: return launch_bn<128, true, true>(g, p, s);
+    case 64: return launch_bn<64, false, false>(g, p, s);
+    case 65: return launch_bn<64, true, false>(g, p, s);
+    case 66: return launch_bn<64, false, true>(g, p, s);
+    case 67: return launch_bn<64, true, true>(g, p, s);
+    default: set_error("gemm: no kernel for tile width %d", g.bn); return SV_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s, int part) {
   if (e.out != g.out || e.out_e4m3 != g.out_e4m3 || e.residual != g.res) {
     set_error("gemm: epilogue buffers differ from the ones the tensor maps were built for");
     return SV_ERR_INVALID_ARG;
   }
+  const bool split = g.k_splits > 1;
   Params p;
   p.M = g.M;
   p.N = g.N;
@@ -937,7 +1208,7 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
   p.blk_col0 = e.blk_col0;
   p.blk_qk8 = e.blk_qk8;
   p.ln_part = e.ln_part;
-  if (e.ln_part && (e.blk_out || 2 * p.n_tiles > kMaxLnTiles || (g.fp8 && g.mc))) {
+  if (e.ln_part && (e.blk_out || 2 * p.n_tiles > kMaxLnTiles || (g.fp8 && g.mc && !split))) {
     set_error("gemm: row statistics need a row-major output of at most %d column tiles (and not E4M3 operands "
               "with CTA pairs)", kMaxLnTiles / 2);
     return SV_ERR_INVALID_ARG;
@@ -953,27 +1224,46 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s) {
     return SV_ERR_INVALID_ARG;
   }
   p.err = dev_err();
-  const int key = g.bn | (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0) | (g.atoms == 2 ? 4 : 0);
-  switch (key) {
-    case 256: return launch_bn<256, false, false>(g, p, s);
-    case 257: return launch_bn<256, true, false>(g, p, s);
-    case 258: return launch_bn<256, false, true>(g, p, s);
-    case 259: return launch_bn<256, true, true>(g, p, s);
-    case 262: return launch_bn<256, false, true, 2>(g, p, s);
-    case 192: return launch_bn<192, false, false>(g, p, s);
-    case 193: return launch_bn<192, true, false>(g, p, s);
-    case 194: return launch_bn<192, false, true>(g, p, s);
-    case 195: return launch_bn<192, true, true>(g, p, s);
-    case 128: return launch_bn<128, false, false>(g, p, s);
-    case 129: return launch_bn<128, true, false>(g, p, s);
-    case 130: return launch_bn<128, false, true>(g, p, s);
-    case 131: return launch_bn<128, true, true>(g, p, s);
-    case 64: return launch_bn<64, false, false>(g, p, s);
-    case 65: return launch_bn<64, true, false>(g, p, s);
-    case 66: return launch_bn<64, false, true>(g, p, s);
-    case 67: return launch_bn<64, true, true>(g, p, s);
-    default: set_error("gemm: no kernel for tile width %d", g.bn); return SV_ERR_UNSUPPORTED;
+  p.k_splits = split ? g.k_splits : 1;
+  p.kb_split = split ? g.kb_split : 0;
+  p.ws_m_tiles = g.mc ? 2 * ((p.m_tiles + 1) / 2) : p.m_tiles;
+  if (!split) return part == 1 ? SV_OK : launch_main(g, p, s, false);
+  if (!e.ws || e.ws != g.ws || e.ln_r || e.blk_out || g.bn != 256) {
+    set_error("gemm: a split-K GEMM needs the partial-sum workspace its maps were built for and a row-major "
+              "output without a folded LayerNorm");
+    return SV_ERR_INVALID_ARG;
   }
+  if (part != 1) {  // the K ranges' raw sums; the epilogue runs in the reduction
+    Params pm = p;
+    pm.has_res = 0;
+    pm.bias = nullptr;
+    pm.pos = nullptr;
+    pm.ln_part = nullptr;
+    pm.act = SV_ACT_NONE;
+    sv_status st = launch_main(g, pm, s, true);
+    if (st != SV_OK || part == 0) return st;
+  }
+  ReduceParams q;
+  q.ws = e.ws;
+  q.k_splits = g.k_splits;
+  q.m_pad = p.ws_m_tiles * kBM;
+  q.n_pad = p.n_tiles * g.bn;
+  q.n_tiles = p.n_tiles;
+  q.M = g.M;
+  q.N = g.N;
+  q.scale = e.scale;
+  q.bias = e.bias;
+  q.pos = e.pos;
+  q.pos_rows = p.pos_rows;
+  q.res = e.residual;
+  q.act = e.act;
+  q.out_e4m3 = e.out_e4m3;
+  q.out = e.out;
+  q.ln_part = e.ln_part;
+  const long warps = long(g.M) * p.n_tiles;
+  cudaError_t ce = launch_pdl(gemm_splitk_reduce_kernel, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, s, q);
+  if (ce != cudaSuccess) return cuda_fail(ce, "gemm split-K reduction launch");
+  return SV_OK;
 }
 
 }  // namespace sv

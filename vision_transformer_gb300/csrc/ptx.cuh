@@ -442,6 +442,16 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 }
 
 // max(a, b, c) in one instruction
+// Pairwise update of count / mean / sum of squared deviations (Chan et al.):
+// (n, mean, m2) <- merge with (nb, mb, m2b); a side with no columns leaves the other.
+__device__ __forceinline__ void chan_merge(float& n, float& mean, float& m2, float nb, float mb, float m2b) {
+  if (nb == 0.0f) return;
+  const float nn = n + nb, d = mb - mean, f = __fdividef(nb, nn);
+  mean = fmaf(d, f, mean);
+  m2 += m2b + d * d * (n * f);
+  n = nn;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

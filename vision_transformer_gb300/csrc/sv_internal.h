@@ -84,6 +84,9 @@ struct GemmEpi {
   // mean) of those F32 results (after bias, positions and residual).
   // ln_finalize_launch merges them.
   float2* ln_part = nullptr;
+  // Partial sums of a GEMM that splits K (GemmOperands::k_splits > 1): at least
+  // gemm_splitk_ws_bytes(g) bytes, used by gemm_launch and free again when its work ends.
+  float* ws = nullptr;
 };
 // Statistics entries per row that GemmEpi::ln_part can hold (two per column tile:
 // 1152 columns in tiles of >= 64).
@@ -95,6 +98,7 @@ struct GemmOperands {
   CUtensorMap tw_tail;         // W rows of the narrow last column tile (CTA pairs)
   CUtensorMap ta_aug, tw_aug;  // the extra K block of a folded LayerNorm
   CUtensorMap tw_aug_tail;     // its W rows for the narrow last column tile (CTA pairs)
+  CUtensorMap tws;             // split-K partial-sum workspace (row-major F32)
   int has_aug = 0;
   int tail_n = 0;              // MMA N of the narrow last column tile, 0 if all tiles are full
   int tail_last = 0;           // narrow tiles after all full ones in the work order
@@ -103,22 +107,32 @@ struct GemmOperands {
   int bn = 0;
   int mc = 0;  // CTA pairs (clusters of 2) sharing one 256-row MMA
   int atoms = 1;  // 128-byte swizzle rows of K per pipeline stage (1 or 2)
+  int k_splits = 1;  // K ranges run by separate CTAs (pairs), summed by a reduction kernel
+  int kb_split = 0;  // pipeline stages of K per range
   int has_res = 0;
   const void* out = nullptr;  // epilogue buffers the output / residual maps describe
   const void* res = nullptr;
+  const float* ws = nullptr;  // the split-K workspace the map tws describes
   int out_e4m3 = 0;
 };
 
 // Tensor map of a K-major operand [rows, K] (row stride = K elements) with the
 // 128-byte swizzle the GEMM expects, box [box_rows, 128 bytes].
 sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int fp8, int box_rows);
-int gemm_pick_bn(int M, int N, int K, bool mc);
-// allow_pair = false keeps single-CTA tiles.
+int gemm_pick_bn(int M, int N, int K, bool mc, double* t_best = nullptr);
+// allow_pair = false keeps single-CTA tiles; max_splits > 1 lets a small-M, long-K GEMM
+// split K into up to that many ranges (the caller then provides GemmEpi::ws).
 sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8,
-                       bool allow_pair = true);
+                       bool allow_pair = true, int max_splits = 1);
+// Workspace bytes of a prepared GEMM's split-K partial sums (0 without a split), and the
+// same for the shape that gemm_prepare(..., true, max_splits) would choose.
+size_t gemm_splitk_ws_bytes(const GemmOperands& g);
+size_t gemm_splitk_ws_bytes_for(int M, int N, int K, int fp8, int max_splits);
 // Builds the output / residual tensor maps for the epilogue's buffers (must precede gemm_launch).
 sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e);
-sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s);
+// part: -1 every launch; with split K, 0 only the GEMM and 1 only the reduction (each
+// with its own launch accounting).
+sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s, int part = -1);
 
 // Launches kern with programmatic stream serialization (the kernel must call
 // pdl_wait() before touching global memory; see ptx.cuh).
