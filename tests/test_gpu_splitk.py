@@ -135,3 +135,44 @@ def test_encoder_batch1_split_mlp_down_and_statistics(sv, two_layers):
     qkv2 = _stage(sv, pix_dev, 2, sv.SV_STAGE_QKV, 3 * D)
     ref = oracle.linear(oracle.layernorm(f16(x1), p["ln1_g"][1], p["ln1_b"][1]), p["qkv_w"][1], p["qkv_b"][1])
     assert_close(qkv2, ref, RT, 2 * RT * _scale(ref), "layer 2 LN1 (statistics from the split reduction) + QKV")
+
+
+def test_tail_split_gemm(sv):
+    """The MLP-down shape at 32 images (23,328 x 1152 x 4304): 460 pair tiles on 76
+    CTA pairs leave 4 for a seventh round, whose K is split over the idle pairs (two
+    launches). Rows of whole tiles (the first 64) and of the split last tiles (the last
+    64, whose columns 256.. are split) against the oracle on those rows."""
+    M, N, K = 23328, 1152, 4304
+    A, W, b = _inputs(76, M, N, K)
+    R = synth.normal(76, 4, (M, N))
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    assert _launches(sv, lambda: sv.sv_gemm_bias_act(dev_f16(A), dev_f16(W.T), dev_f16(b), None, 1, dev_f16(R), C, M,
+                                                     N, K)) == 2
+    got = host(C)
+    for rows in (slice(0, 64), slice(M - 64, M)):
+        ref = oracle.linear(A[rows], W, b, residual=R[rows])
+        assert_close(got[rows], ref, RT, RT * _scale(ref), f"tail split rows {rows}")
+
+
+def test_encoder_batch32_tail_split_statistics(sv, two_layers):
+    """32 images, F16: the MLP-down projection splits its last round's tiles; layer 2's
+    folded LayerNorm reads row statistics from both the whole tiles' epilogues and the
+    reduction. Layer 2's LN1 + QKV against the oracle on the GPU's X after layer 1, on
+    rows of both kinds."""
+    p, _ = two_layers
+    B = 32
+    pix = torch.from_numpy(synth.pixels(6, B)).cuda()
+    f16 = lambda a: np.asarray(a, dtype=np.float64).astype(np.float16)
+
+    def stage(layers, st, cols):
+        dst = torch.full((B * T, cols), float("nan"), dtype=torch.float16, device="cuda")
+        sv.sv_debug_encode_stage(pix, B, layers, 0, 0, st, dst, dst.numel() * 2)
+        sv.sv_sync()
+        return host(dst)
+
+    x1 = stage(1, sv.SV_STAGE_MLP_DOWN, D)
+    qkv2 = stage(2, sv.SV_STAGE_QKV, 3 * D)
+    for rows in (slice(0, 64), slice(B * T - 64, B * T)):
+        ref = oracle.linear(oracle.layernorm(f16(x1[rows]), p["ln1_g"][1], p["ln1_b"][1]), p["qkv_w"][1],
+                            p["qkv_b"][1])
+        assert_close(qkv2[rows], ref, RT, 2 * RT * _scale(ref), f"layer 2 LN1 + QKV rows {rows}")

@@ -25,9 +25,10 @@
 //               TMA store; residual blocks arrive by TMA one chunk ahead; the
 //               GEMMs that write the residual stream also leave per-tile row
 //               statistics for the next LayerNorm.
-// Split K (small M, long K: tiles that would fill few SMs): the work items are
-// (tile, K range) pairs; each writes its raw F32 sums to a workspace and
-// gemm_splitk_reduce_kernel adds them up in a fixed order and applies the epilogue.
+// Split K (long K): at small M, where the tiles would fill few SMs, every tile, and
+// otherwise the tiles of a short last wave, become (tile, K range) items; each writes
+// its raw F32 sums to a workspace and gemm_splitk_reduce_kernel adds them up in a
+// fixed order and applies the epilogue.
 // Launched with programmatic stream serialization: the prologue overlaps the
 // previous kernel, global memory is touched only after griddepcontrol.wait.
 // F16 operands use kind::f16 (K = 16 per instruction); E4M3 operands use
@@ -126,11 +127,11 @@ struct Params {
   int blk_col0;  // first column of the fused [Q | K | V] space this GEMM's columns start at
   int blk_qk8;   // Q and K as E4M3 (16 x value): 16-byte groups of 16 columns per row
   float2* ln_part;  // per (row, column tile): (mean, M2) of the results, or null
-  // split K: item = tile * k_splits + split; split s runs the K blocks
-  // [s kb_split, min(k_blocks, (s + 1) kb_split)) and stores its raw sums in rows
-  // s * ws_m_tiles * 128 + (tile row) of the row-major F32 workspace (through tmC)
-  int k_splits, kb_split;
-  int ws_m_tiles;
+  // split K: items below n_main are whole tiles; item n_main + q * k_splits + s is K
+  // range s (K blocks [s kb_split, min(k_blocks, (s + 1) kb_split))) of tile item
+  // n_main + q, whose raw sums go to rows ((q * k_splits + s) * (PAIR ? 2 : 1) + rank) * 128
+  // .. + 127 of the [rows, BN] F32 workspace (through tmAa)
+  int n_main, k_splits, kb_split;
 };
 
 // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), with
@@ -189,25 +190,33 @@ __device__ __forceinline__ int tile_chunks(const Params& p, int nt, int bn) {
 // then fills the last wave. With PAIR an item is a 256-row
 // tile of two vertically adjacent 128-row tiles; the CTA of cluster rank r takes
 // m-tile 2 * pair + r.
-template <bool PAIR>
-__device__ __forceinline__ void tile_of(const Params& p, int it, int rank, int& mt, int& nt) {
-  const int full_items = (PAIR ? (p.m_tiles + 1) / 2 : p.m_tiles) * p.n_full;
-  int mu;
-  if (!p.tail_last) {  // row by row: the tiles of one row share their A rows in L2
-    mu = it / p.n_tiles;
-    nt = it - mu * p.n_tiles;
+// mu: the 128-row tile (PAIR: the 256-row pair of tiles) of tile item `it`.
+__host__ __device__ __forceinline__ void tile_pos(int it, int row_units, int n_tiles, int n_full, int tail_last,
+                                                  int& mu, int& nt) {
+  const int full_items = row_units * n_full;
+  if (!tail_last) {  // row by row: the tiles of one row share their A rows in L2
+    mu = it / n_tiles;
+    nt = it - mu * n_tiles;
   } else if (it < full_items) {
-    mu = it / p.n_full;
-    nt = it - mu * p.n_full;
+    mu = it / n_full;
+    nt = it - mu * n_full;
   } else {  // the narrow last column, after every full tile: it fills the last wave
     mu = it - full_items;
-    nt = p.n_full;
+    nt = n_full;
   }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tile_of(const Params& p, int it, int rank, int& mt, int& nt) {
+  int mu;
+  tile_pos(it, PAIR ? (p.m_tiles + 1) / 2 : p.m_tiles, p.n_tiles, p.n_full, p.tail_last, mu, nt);
   mt = PAIR ? 2 * mu + rank : mu;
 }
 
-// SPLIT: items are (tile, K range) pairs whose raw sums go to the split-K workspace.
-template <int BN, bool FP8, bool PAIR, int ATOMS, bool SPLIT>
+// SPLIT: 0 whole tiles only; otherwise the items from n_main on are (tile, K range) pairs
+// whose raw sums go to the split-K workspace (tmAa describes it; no LayerNorm is folded
+// into a split GEMM): 1 every item (n_main = 0), 2 whole tiles first, then split ones.
+template <int BN, bool FP8, bool PAIR, int ATOMS, int SPLIT>
 __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmWt, const __grid_constant__ CUtensorMap tmC,
@@ -242,12 +251,23 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
   const bool leader = rank == 0;
   const int it0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
   const int it_step = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
-  const int k_splits = SPLIT ? p.k_splits : 1;
-  const int num_items = (PAIR ? ((p.m_tiles + 1) / 2) * p.n_tiles : p.m_tiles * p.n_tiles) * k_splits;
-  // K blocks of item it: [kb_lo, kb_hi)
-  auto k_range = [&](int it, int& kb_lo, int& kb_hi) {
-    if (SPLIT) {
-      kb_lo = (it % k_splits) * p.kb_split;
+  const int tile_items = PAIR ? ((p.m_tiles + 1) / 2) * p.n_tiles : p.m_tiles * p.n_tiles;
+  const int main_items = SPLIT == 1 ? 0 : (SPLIT == 2 ? p.n_main : tile_items);  // items that are whole tiles
+  const int num_items = SPLIT ? main_items + (tile_items - main_items) * p.k_splits : tile_items;
+  // item -> tile item; ks = its K range (-1: the whole of K)
+  auto item_tile = [&](int it, int& ks) {
+    if (!SPLIT || it < main_items) {
+      ks = -1;
+      return it;
+    }
+    const int j = it - main_items;
+    ks = j % p.k_splits;
+    return main_items + j / p.k_splits;
+  };
+  // K blocks of K range ks: [kb_lo, kb_hi)
+  auto k_range = [&](int ks, int& kb_lo, int& kb_hi) {
+    if (SPLIT && ks >= 0) {
+      kb_lo = ks * p.kb_split;
       kb_hi = min(p.k_blocks, kb_lo + p.kb_split);
     } else {
       kb_lo = 0;
@@ -299,9 +319,9 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
       uint32_t issued = 0, issued_phase = 0;  // stages with loads in flight, and their phase bit
       bool ok = true;
       for (int it = it0; it < num_items && ok; it += it_step) {
-        int mt, nt, kb_lo, kb_hi;
-        tile_of<PAIR>(p, it / k_splits, rank, mt, nt);
-        k_range(it, kb_lo, kb_hi);
+        int mt, nt, kb_lo, kb_hi, ks;
+        tile_of<PAIR>(p, item_tile(it, ks), rank, mt, nt);
+        k_range(ks, kb_lo, kb_hi);
         for (int kb = kb_lo; kb < kb_hi + aug_blocks; ++kb) {
           if (!mbar_wait<kSleepProducer>(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.err)) {
             ok = false;
@@ -387,9 +407,9 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
       for (int it = it0; it < num_items && ok; it += it_step, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        int mt_i, nt_i, kb_lo, kb_hi;
-        tile_of<PAIR>(p, it / k_splits, rank, mt_i, nt_i);
-        k_range(it, kb_lo, kb_hi);
+        int mt_i, nt_i, kb_lo, kb_hi, ks;
+        tile_of<PAIR>(p, item_tile(it, ks), rank, mt_i, nt_i);
+        k_range(ks, kb_lo, kb_hi);
         const uint32_t idesc = (nt_i == p.n_full && p.tail_n) ? idesc_tail : idesc_full;
         if (!mbar_wait<kSleepMma>(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
@@ -478,9 +498,9 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
     // prefetch cursor: next chunk whose residual is to be loaded (work item, chunk, counter)
     int pit = it0, pc = part, pq = 0;
     auto prefetch_upto = [&](int qmax) {  // issue residual loads for chunks pq .. qmax
-      while (p.has_res && pq <= qmax && pit < num_items) {
+      while (p.has_res && pq <= qmax && pit < main_items) {  // split items read no residual
         int mt2, nt2;
-        tile_of<PAIR>(p, pit / k_splits, rank, mt2, nt2);
+        tile_of<PAIR>(p, pit, rank, mt2, nt2);
         if (pc >= tile_chunks(p, nt2, BN)) {  // no (more) chunks of this warp in the tile
           pc = part;
           pit += it_step;
@@ -506,8 +526,9 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
     bool ok = true;
     const uint32_t tempty_lead0 = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
     for (int it = it0; it < num_items && ok; it += it_step, ++local) {
-      int mt, nt;
-      tile_of<PAIR>(p, it / k_splits, rank, mt, nt);
+      int mt, nt, ks;
+      const int ti = item_tile(it, ks);
+      tile_of<PAIR>(p, ti, rank, mt, nt);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const int row0 = mt * kBM + sub * 32;
@@ -521,9 +542,9 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
       if (!__all_sync(0xffffffffu, mbar_wait<kSleepEpi>(bar_tfull + 8 * acc, acc_phase, abort_flag, p.err))) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + uint32_t(acc * BN) + (uint32_t(sub * 32) << 16);
-      if (SPLIT) {  // this K range's raw sums: each 32 x 32 F32 chunk staged in the warp's
-                    // 4 KB (128-byte swizzle) and written by one TMA store to the workspace
-        const int wrow = ((it % k_splits) * p.ws_m_tiles + mt) * kBM + sub * 32;
+      if (SPLIT && ks >= 0) {  // this K range's raw sums: each 32 x 32 F32 chunk staged in the
+                               // warp's 4 KB (128-byte swizzle), one TMA store to the workspace
+        const int wrow = (((ti - main_items) * p.k_splits + ks) * (PAIR ? 2 : 1) + rank) * kBM + sub * 32;
         for (int c = part; c < nch; c += kParts) {
           if (lane == 0) bulk_wait_read<0>();  // the previous chunk's store has read the block
           __syncwarp();
@@ -537,7 +558,7 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmC, smem_u32(ring), nt * BN + 32 * c, wrow);
+            tma_store_2d(&tmAa, smem_u32(ring), 32 * c, wrow);
             bulk_commit();
           }
         }
@@ -742,7 +763,9 @@ __global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
 // merged across lanes) for the next LayerNorm.
 struct ReduceParams {
   const float* ws;
-  int k_splits, m_pad, n_pad, n_tiles;  // workspace: k_splits x [m_pad, n_pad] F32, 256-wide tiles
+  int k_splits, n_main, n_split;  // split tiles: tile items n_main .. n_main + n_split - 1
+  int row_units, rows_per;  // 128-row tiles or 256-row pairs, and their rows (128 / 256)
+  int n_tiles, n_full, tail_last;
   int M, N;
   float scale;
   const __half* bias;
@@ -758,11 +781,18 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const ReducePar
   pdl_launch_dependents();
   pdl_wait();  // the partial sums come from the GEMM launched just before
   const int lane = threadIdx.x & 31;
-  const long wid = (long(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (wid >= long(q.M) * q.n_tiles) return;  // whole warps
-  const int row = int(wid / q.n_tiles), nt = int(wid - long(row) * q.n_tiles);
+  const long wid = (long(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;  // (split tile, row of it)
+  const int qt = int(wid / q.rows_per), r = int(wid - long(qt) * q.rows_per);
+  if (qt >= q.n_split) return;  // whole warps
+  int mu, nt;
+  tile_pos(q.n_main + qt, q.row_units, q.n_tiles, q.n_full, q.tail_last, mu, nt);
+  const int row = mu * q.rows_per + r;
+  if (row >= q.M) return;  // whole warps
   const int col = nt * 256 + 8 * lane;
   const bool live = col < q.N;  // N is a multiple of 16: all eight columns exist
+  // this row's sums of K range s: workspace row (qt * k_splits + s) * rows_per + r
+  const float* wsr = q.ws + (size_t(qt) * q.k_splits * q.rows_per + r) * 256 + 8 * lane;
+  const size_t s_stride = size_t(q.rows_per) * 256;
   float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
   if (live) {
     float4 a[2 * 8];
@@ -770,7 +800,7 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const ReducePar
 #pragma unroll
     for (int s = 0; s < 8; ++s)
       if (s < ns) {
-        const float4* src = reinterpret_cast<const float4*>(q.ws + (size_t(s) * q.m_pad + row) * q.n_pad + col);
+        const float4* src = reinterpret_cast<const float4*>(wsr + s * s_stride);
         a[2 * s] = __ldg(src);
         a[2 * s + 1] = __ldg(src + 1);
       }
@@ -781,7 +811,7 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const ReducePar
         v[4] += a[2 * s + 1].x, v[5] += a[2 * s + 1].y, v[6] += a[2 * s + 1].z, v[7] += a[2 * s + 1].w;
       }
     for (int s = 8; s < q.k_splits; ++s) {
-      const float4* src = reinterpret_cast<const float4*>(q.ws + (size_t(s) * q.m_pad + row) * q.n_pad + col);
+      const float4* src = reinterpret_cast<const float4*>(wsr + s * s_stride);
       const float4 x = __ldg(src), y = __ldg(src + 1);
       v[0] += x.x, v[1] += x.y, v[2] += x.z, v[3] += x.w, v[4] += y.x, v[5] += y.y, v[6] += y.z, v[7] += y.w;
     }
@@ -840,7 +870,7 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const ReducePar
   }
 }
 
-template <int BN, bool FP8, bool PAIR, int ATOMS = 1, bool SPLIT = false>
+template <int BN, bool FP8, bool PAIR, int ATOMS = 1, int SPLIT = 0>
 sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
   using C = Cfg<BN, PAIR, ATOMS, epi_warps<FP8, PAIR>()>;
   auto kern = gemm_tc_kernel<BN, FP8, PAIR, ATOMS, SPLIT>;
@@ -855,7 +885,9 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm)");
     attr_set |= bit;
   }
-  const int items = (PAIR ? ((prm.m_tiles + 1) / 2) * prm.n_tiles : prm.m_tiles * prm.n_tiles) * (SPLIT ? prm.k_splits : 1);
+  const int tile_items = PAIR ? ((prm.m_tiles + 1) / 2) * prm.n_tiles : prm.m_tiles * prm.n_tiles;
+  const int n_main = SPLIT == 1 ? 0 : prm.n_main;
+  const int items = SPLIT ? n_main + (tile_items - n_main) * prm.k_splits : tile_items;
   const int slots = PAIR ? num_sms() / 2 : num_sms();  // one CTA (PAIR: one two-CTA cluster) per SM (pair)
   const int units = items < slots ? items : slots;
   cudaLaunchConfig_t cfg = {};
@@ -878,13 +910,13 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  const CUtensorMap& tcm = SPLIT ? g.tws : g.tc;  // split K: the workspace takes the output's place
-  const CUtensorMap& tr = g.has_res ? g.tr : tcm;
+  const CUtensorMap& tr = g.has_res ? g.tr : g.tc;
   const CUtensorMap& twt = (PAIR && g.tail_n) ? g.tw_tail : g.tw;
-  const CUtensorMap& taa = prm.ln_aug ? g.ta_aug : g.ta;
+  // split K: the workspace map takes the place of the (unused) folded-LayerNorm A block
+  const CUtensorMap& taa = SPLIT ? g.tws : (prm.ln_aug ? g.ta_aug : g.ta);
   const CUtensorMap& twa = prm.ln_aug ? g.tw_aug : g.tw;
   const CUtensorMap& twat = (prm.ln_aug && PAIR && g.tail_n) ? g.tw_aug_tail : twa;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, g.ta, g.tw, twt, tcm, tr, taa, twa, twat, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, g.ta, g.tw, twt, g.tc, tr, taa, twa, twat, prm);
   if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
   return SV_OK;
 }
@@ -1002,6 +1034,41 @@ int pick_splits(int M, int N, int K, int fp8, bool allow_pair, int max_splits, d
   return splits;
 }
 
+// Split the tiles of a short last wave. When a long-K GEMM's tiles fill all CTAs
+// (pairs) for some waves and then only a few of them, the last round runs those few
+// tiles at whole K while the rest wait (the 23,328 x 1152 x 4304 MLP-down projection:
+// 460 pair tiles on 76 pairs, 4 in the seventh round). Their K is split over the idle
+// pairs instead and the reduction finishes them. Measured on that shape: 161.1 -> 152.1
+// us with F16 operands (the whole step at 32 images 0.9% faster), a round of one narrow
+// tile (128 columns, 93,312 rows) no gain, and E4M3 99.2 -> 102.2 us (its main loop is
+// short against the epilogue); so F16 only, and only when the round shortens by more than
+// three reductions (gemm_pick_bn's time units, as pick_splits).
+void pick_tail_split(GemmOperands* g, int k_blocks) {
+  constexpr double kReduceCost = 125.0;
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  if (g->fp8 || g->K < 2048 || g->bn != 256 || g->atoms != 1) return;
+  const int mt = (g->M + kBM - 1) / kBM, units = g->mc ? (mt + 1) / 2 : mt;
+  const int n_tiles = (g->N + g->bn - 1) / g->bn, n_full = g->tail_n ? n_tiles - 1 : n_tiles;
+  const int items = units * n_tiles, slots = g->mc ? sms / 2 : sms;
+  const int rem = items % slots;
+  if (items < slots || rem == 0 || rem * 8 > slots) return;
+  int splits = slots / rem;
+  if (splits > 8) splits = 8;
+  if (splits > k_blocks / 8) splits = k_blocks / 8;
+  if (splits < 2) return;
+  int width = 0;  // the widest tile of the last round
+  for (int it = items - rem; it < items; ++it) {
+    int mu, nt;
+    tile_pos(it, units, n_tiles, n_full, g->tail_last, mu, nt);
+    const int w = (nt == n_full && g->tail_n) ? g->tail_n : g->bn;
+    width = w > width ? w : width;
+  }
+  const double t_tile = double(width) / 1780.0 * double(g->K);
+  if (t_tile * (1.0 - 1.0 / splits) <= 3.0 * kReduceCost) return;
+  g->k_splits = splits;
+  g->n_main = items - rem;
+}
+
 // Tile, pairing, stage and split choices for an M x N x K GEMM (no tensor maps).
 void gemm_choose(GemmOperands* g, int M, int N, int K, int fp8, bool allow_pair, int max_splits) {
   g->M = M;
@@ -1026,12 +1093,7 @@ void gemm_choose(GemmOperands* g, int M, int N, int K, int fp8, bool allow_pair,
   // empty, and with the E4M3 pairs' wider epilogue only two 64 KB stages would fit.
   g->atoms = (!fp8 && g->mc && g->bn == 256 && K <= 2048 && K % (2 * kSwzBytes / 2) == 0 && g->k_splits == 1) ? 2 : 1;
   g->kb_split = 0;
-  if (g->k_splits > 1) {  // equal ranges of whole stages; no range is empty
-    const int bk = (fp8 ? kSwzBytes : kSwzBytes / 2) * g->atoms;
-    const int k_blocks = (K + bk - 1) / bk;
-    g->kb_split = (k_blocks + g->k_splits - 1) / g->k_splits;
-    g->k_splits = (k_blocks + g->kb_split - 1) / g->kb_split;
-  }
+  g->n_main = 0;  // with a small-M split every tile is split
 
   // A narrower last column tile (N % bn columns) runs MMAs of its own width, rounded
   // up to 16 columns (32 for a CTA pair, whose CTAs hold half of the W rows each).
@@ -1064,15 +1126,22 @@ void gemm_choose(GemmOperands* g, int M, int N, int K, int fp8, bool allow_pair,
     const double a_bytes = double(M) * K * (fp8 ? 1 : 2);
     if (units > 0 && a_bytes <= 64e6 && makespan(true) * 20 <= makespan(false) * 19) g->tail_last = 1;
   }
+  const int bk = (fp8 ? kSwzBytes : kSwzBytes / 2) * g->atoms;
+  const int k_blocks = (K + bk - 1) / bk;
+  if (g->k_splits == 1 && max_splits > 1) pick_tail_split(g, k_blocks);
+  if (g->k_splits > 1) {  // equal ranges of whole stages; no range is empty
+    g->kb_split = (k_blocks + g->k_splits - 1) / g->k_splits;
+    g->k_splits = (k_blocks + g->kb_split - 1) / g->kb_split;
+  }
 }
 
 }  // namespace
 
 size_t gemm_splitk_ws_bytes(const GemmOperands& g) {
   if (g.k_splits <= 1) return 0;
-  const int mt = (g.M + kBM - 1) / kBM, m_tiles = g.mc ? 2 * ((mt + 1) / 2) : mt;
-  const int n_tiles = (g.N + g.bn - 1) / g.bn;
-  return size_t(g.k_splits) * m_tiles * n_tiles * size_t(kBM) * g.bn * sizeof(float);
+  const int mt = (g.M + kBM - 1) / kBM, units = g.mc ? (mt + 1) / 2 : mt;
+  const int n_split = units * ((g.N + g.bn - 1) / g.bn) - g.n_main;
+  return size_t(n_split) * g.k_splits * (g.mc ? 2 : 1) * size_t(kBM) * g.bn * sizeof(float);
 }
 
 size_t gemm_splitk_ws_bytes_for(int M, int N, int K, int fp8, int max_splits) {
@@ -1127,11 +1196,10 @@ sv_status gemm_bind_epilogue(GemmOperands* g, const GemmEpi& e) {
   g->out_e4m3 = e.out_e4m3;
   g->res = e.residual;
   g->ws = nullptr;
-  if (g->k_splits > 1 && e.ws) {  // split K: [k_splits * m_pad, n_pad] F32, 32 x 32 blocks, 128-byte swizzle
-    const int mt = (g->M + kBM - 1) / kBM, m_pad = (g->mc ? 2 * ((mt + 1) / 2) : mt) * kBM;
-    const int n_pad = (g->N + g->bn - 1) / g->bn * g->bn;
-    const uint64_t dims[2] = {uint64_t(n_pad), uint64_t(g->k_splits) * uint64_t(m_pad)};
-    const uint64_t strides[1] = {uint64_t(n_pad) * 4u};
+  if (g->k_splits > 1 && e.ws) {  // split K: [rows, BN] F32 (Params), 32 x 32 blocks, 128-byte swizzle
+    const uint64_t rows = gemm_splitk_ws_bytes(*g) / (sizeof(float) * size_t(g->bn));
+    const uint64_t dims[2] = {uint64_t(g->bn), rows};
+    const uint64_t strides[1] = {uint64_t(g->bn) * 4u};
     const uint32_t box[2] = {32, 32};
     st = make_tmap(&g->tws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, e.ws, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != SV_OK) return st;
@@ -1145,13 +1213,15 @@ namespace {
 
 sv_status launch_main(const GemmOperands& g, const Params& p, cudaStream_t s, bool split) {
   if (split) {  // split K: 256-wide tiles, one swizzle row of K per stage (gemm_choose)
-    const int key = (g.bn == 256 && g.atoms == 1) ? (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0) : -1;
+    const int key = (g.bn == 256 && g.atoms == 1) ? (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0) | (g.n_main ? 4 : 0) : -1;
     switch (key) {
-      case 0: return launch_bn<256, false, false, 1, true>(g, p, s);
-      case 1: return launch_bn<256, true, false, 1, true>(g, p, s);
-      case 2: return launch_bn<256, false, true, 1, true>(g, p, s);
-      case 3: return launch_bn<256, true, true, 1, true>(g, p, s);
-      default: set_error("gemm: no split-K kernel for tile width %d", g.bn); return SV_ERR_UNSUPPORTED;
+      case 0: return launch_bn<256, false, false, 1, 1>(g, p, s);
+      case 1: return launch_bn<256, true, false, 1, 1>(g, p, s);
+      case 2: return launch_bn<256, false, true, 1, 1>(g, p, s);
+      case 3: return launch_bn<256, true, true, 1, 1>(g, p, s);
+      case 4: return launch_bn<256, false, false, 1, 2>(g, p, s);  // a split last round (F16 only)
+      case 6: return launch_bn<256, false, true, 1, 2>(g, p, s);
+      default: set_error("gemm: no split-K kernel for this configuration"); return SV_ERR_UNSUPPORTED;
     }
   }
   const int key = g.bn | (g.fp8 ? 1 : 0) | (g.mc ? 2 : 0) | (g.atoms == 2 ? 4 : 0);
@@ -1208,7 +1278,9 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s, i
   p.blk_col0 = e.blk_col0;
   p.blk_qk8 = e.blk_qk8;
   p.ln_part = e.ln_part;
-  if (e.ln_part && (e.blk_out || 2 * p.n_tiles > kMaxLnTiles || (g.fp8 && g.mc && !split))) {
+  // (E4M3 pair kernels run three epilogue warps per lane quarter, which keep no statistics:
+  // only a GEMM whose every tile is split, and so reduced, can give them)
+  if (e.ln_part && (e.blk_out || 2 * p.n_tiles > kMaxLnTiles || (g.fp8 && g.mc && (!split || g.n_main > 0)))) {
     set_error("gemm: row statistics need a row-major output of at most %d column tiles (and not E4M3 operands "
               "with CTA pairs)", kMaxLnTiles / 2);
     return SV_ERR_INVALID_ARG;
@@ -1226,29 +1298,29 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s, i
   p.err = dev_err();
   p.k_splits = split ? g.k_splits : 1;
   p.kb_split = split ? g.kb_split : 0;
-  p.ws_m_tiles = g.mc ? 2 * ((p.m_tiles + 1) / 2) : p.m_tiles;
+  p.n_main = split ? g.n_main : 0;
   if (!split) return part == 1 ? SV_OK : launch_main(g, p, s, false);
   if (!e.ws || e.ws != g.ws || e.ln_r || e.blk_out || g.bn != 256) {
     set_error("gemm: a split-K GEMM needs the partial-sum workspace its maps were built for and a row-major "
               "output without a folded LayerNorm");
     return SV_ERR_INVALID_ARG;
   }
-  if (part != 1) {  // the K ranges' raw sums; the epilogue runs in the reduction
-    Params pm = p;
-    pm.has_res = 0;
-    pm.bias = nullptr;
-    pm.pos = nullptr;
-    pm.ln_part = nullptr;
-    pm.act = SV_ACT_NONE;
-    sv_status st = launch_main(g, pm, s, true);
+  if (part != 1) {  // whole tiles with their epilogue, and the split tiles' K ranges' raw sums
+    sv_status st = launch_main(g, p, s, true);
     if (st != SV_OK || part == 0) return st;
   }
+  // the split tiles: their ranges' sums added up and the epilogue
+  const int units = g.mc ? (p.m_tiles + 1) / 2 : p.m_tiles;
   ReduceParams q;
   q.ws = e.ws;
   q.k_splits = g.k_splits;
-  q.m_pad = p.ws_m_tiles * kBM;
-  q.n_pad = p.n_tiles * g.bn;
+  q.n_main = g.n_main;
+  q.n_split = units * p.n_tiles - g.n_main;
+  q.row_units = units;
+  q.rows_per = g.mc ? 2 * kBM : kBM;
   q.n_tiles = p.n_tiles;
+  q.n_full = p.n_full;
+  q.tail_last = p.tail_last;
   q.M = g.M;
   q.N = g.N;
   q.scale = e.scale;
@@ -1260,7 +1332,7 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s, i
   q.out_e4m3 = e.out_e4m3;
   q.out = e.out;
   q.ln_part = e.ln_part;
-  const long warps = long(g.M) * p.n_tiles;
+  const long warps = long(q.n_split) * q.rows_per;
   cudaError_t ce = launch_pdl(gemm_splitk_reduce_kernel, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, s, q);
   if (ce != cudaSuccess) return cuda_fail(ce, "gemm split-K reduction launch");
   return SV_OK;

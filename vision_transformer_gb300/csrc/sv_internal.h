@@ -109,6 +109,7 @@ struct GemmOperands {
   int atoms = 1;  // 128-byte swizzle rows of K per pipeline stage (1 or 2)
   int k_splits = 1;  // K ranges run by separate CTAs (pairs), summed by a reduction kernel
   int kb_split = 0;  // pipeline stages of K per range
+  int n_main = 0;    // with k_splits > 1: tile items below n_main run whole (the rest split)
   int has_res = 0;
   const void* out = nullptr;  // epilogue buffers the output / residual maps describe
   const void* res = nullptr;
