@@ -545,6 +545,13 @@ sv_status get_plan(int B, int fp8, int flags, Plan** out) {
         (st = make_call(&p->fc2[i], p->Hh, fp8 ? (const void*)w.fc2_w8 : w.fc2_w, Mi, d.D, d.F, fp8, de, d.F, p->ws,
                         p->ws_bytes)))
       return fail(st);
+    // MLP down with every tile split (small batches): its reduction finishes the next
+    // LayerNorm's statistics itself, so the encoder skips that finalize launch
+    if (p->fold_ln && p->fc2[i].g.k_splits > 1 && p->fc2[i].g.n_main == 0 && (d.D + 255) / 256 <= 8) {
+      p->fc2[i].e.ln_part = nullptr;
+      p->fc2[i].e.ln_r_out = p->ln_r;
+      p->fc2[i].e.ln_aug_out = p->ln_aug;
+    }
   }
   *out = p.get();
   g_plans[key] = std::move(p);
@@ -626,8 +633,10 @@ sv_status encode(Plan& p, const __half* pixels, __half* out, int layers, cudaStr
     const LayerW& w = g_w.layers[size_t(l)];
     const size_t i = size_t(l);
     const bool last = l == layers - 1;
-    SV_TRY(p.fold_ln ? run_ln_finalize(p, l == 0 ? p.patch : p.fc2[i - 1], M, s)
-                     : run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
+    // (after a split MLP-down GEMM whose reduction finished the statistics, nothing to do)
+    if (!(p.fold_ln && l > 0 && p.fc2[i - 1].e.ln_r_out))
+      SV_TRY(p.fold_ln ? run_ln_finalize(p, l == 0 ? p.patch : p.fc2[i - 1], M, s)
+                       : run_ln(p.X, w.ln1_g, w.ln1_b, p.Y, M, fp8, s));
     for (int j = 0; j < p.qkv_calls; ++j) SV_TRY(run_gemm(p.qkv[i * size_t(p.qkv_calls) + size_t(j)], s));
     if (last && stop == SV_STAGE_QKV) return SV_OK;
     {

@@ -206,6 +206,13 @@ __host__ __device__ __forceinline__ void tile_pos(int it, int row_units, int n_t
   }
 }
 
+// The inverse of tile_pos: tile item of row unit mu and column tile nt.
+__host__ __device__ __forceinline__ int tile_index(int mu, int nt, int row_units, int n_tiles, int n_full,
+                                                   int tail_last) {
+  if (!tail_last) return mu * n_tiles + nt;
+  return nt < n_full ? mu * n_full + nt : row_units * n_full + mu;
+}
+
 template <bool PAIR>
 __device__ __forceinline__ void tile_of(const Params& p, int it, int rank, int& mt, int& nt) {
   int mu;
@@ -775,19 +782,36 @@ struct ReduceParams {
   int act, out_e4m3;
   void* out;
   float2* ln_part;
+  // ROWSTATS: the whole row's LayerNorm statistics instead of ln_part (every tile split):
+  // ln_r[row] = 1 / sqrt(var + eps), ln_aug[row, 0..15] = (-mean_hi, -mean_hi, -mean_lo, 0, ...)
+  float* ln_r;
+  __half* ln_aug;
+  float eps;
 };
 
+// ROWSTATS: one block per row, warp w = column tile w (N <= 8 * 256), every tile split.
+template <bool ROWSTATS>
 __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const ReduceParams q) {
   pdl_launch_dependents();
   pdl_wait();  // the partial sums come from the GEMM launched just before
   const int lane = threadIdx.x & 31;
-  const long wid = (long(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;  // (split tile, row of it)
-  const int qt = int(wid / q.rows_per), r = int(wid - long(qt) * q.rows_per);
-  if (qt >= q.n_split) return;  // whole warps
-  int mu, nt;
-  tile_pos(q.n_main + qt, q.row_units, q.n_tiles, q.n_full, q.tail_last, mu, nt);
-  const int row = mu * q.rows_per + r;
-  if (row >= q.M) return;  // whole warps
+  int qt, r, row, nt;
+  if (ROWSTATS) {
+    row = int(blockIdx.x);
+    nt = int(threadIdx.x >> 5);
+    const int mu = row / q.rows_per;
+    r = row - mu * q.rows_per;
+    qt = tile_index(mu, nt, q.row_units, q.n_tiles, q.n_full, q.tail_last) - q.n_main;
+  } else {
+    const long wid = (long(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;  // (split tile, row of it)
+    qt = int(wid / q.rows_per);
+    r = int(wid - long(qt) * q.rows_per);
+    if (qt >= q.n_split) return;  // whole warps
+    int mu;
+    tile_pos(q.n_main + qt, q.row_units, q.n_tiles, q.n_full, q.tail_last, mu, nt);
+    row = mu * q.rows_per + r;
+    if (row >= q.M) return;  // whole warps
+  }
   const int col = nt * 256 + 8 * lane;
   const bool live = col < q.N;  // N is a multiple of 16: all eight columns exist
   // this row's sums of K range s: workspace row (qt * k_splits + s) * rows_per + r
@@ -847,7 +871,7 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const ReducePar
       *reinterpret_cast<uint2*>(static_cast<uint8_t*>(q.out) + off) = w;
     }
   }
-  if (q.ln_part) {  // (mean, M2): this lane's columns, its chunk, then the chunks of each parity
+  if (ROWSTATS || q.ln_part) {  // (mean, M2): this lane's columns, its chunk, then the chunks of each parity
     float n = 0.0f, mean = 0.0f, m2 = 0.0f;
     if (live) {
       float sum = 0.0f;
@@ -860,13 +884,34 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const ReducePar
     }
 #pragma unroll
     for (int o = 1; o <= 16; o <<= 1) {
-      if (o == 4) continue;  // lane bit 2 is the chunk's parity: the two halves stay apart
+      if (!ROWSTATS && o == 4) continue;  // lane bit 2 is the chunk's parity: the halves stay apart
       const float nb = __shfl_xor_sync(0xffffffffu, n, o), mb = __shfl_xor_sync(0xffffffffu, mean, o),
                   m2b = __shfl_xor_sync(0xffffffffu, m2, o);
       chan_merge(n, mean, m2, nb, mb, m2b);
     }
-    if ((lane == 0 || lane == 4) && n > 0.0f)
-      q.ln_part[(size_t(row) * q.n_tiles + nt) * 2 + (lane >> 2)] = make_float2(mean, m2);
+    if (!ROWSTATS) {
+      if ((lane == 0 || lane == 4) && n > 0.0f)
+        q.ln_part[(size_t(row) * q.n_tiles + nt) * 2 + (lane >> 2)] = make_float2(mean, m2);
+    } else {  // the row's tiles merged by its first thread, then 1/std and the -mean block
+      __shared__ float3 tile_st[8];
+      if (lane == 0) tile_st[nt] = make_float3(n, mean, m2);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float rn = 0.0f, rm = 0.0f, rm2 = 0.0f;
+        for (int t = 0; t < q.n_tiles; ++t) chan_merge(rn, rm, rm2, tile_st[t].x, tile_st[t].y, tile_st[t].z);
+        q.ln_r[row] = rsqrtf(rm2 / float(q.N) + q.eps);
+        const __half hi = __float2half_rn(-rm);
+        const __half lo = __float2half_rn(-rm - __half2float(hi));
+        uint4 w;
+        __half2* h = reinterpret_cast<__half2*>(&w);
+        h[0] = __halves2half2(hi, hi);
+        h[1] = __halves2half2(lo, __float2half_rn(0.0f));
+        h[2] = h[3] = __float2half2_rn(0.0f);
+        uint4* dst = reinterpret_cast<uint4*>(q.ln_aug + size_t(row) * 16);
+        dst[0] = w;
+        dst[1] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
   }
 }
 
@@ -1305,6 +1350,11 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s, i
               "output without a folded LayerNorm");
     return SV_ERR_INVALID_ARG;
   }
+  if ((e.ln_r_out || e.ln_aug_out) && (!e.ln_r_out || !e.ln_aug_out || e.ln_part || g.n_main || p.n_tiles > 8)) {
+    set_error("gemm: whole-row LayerNorm statistics need every tile split, at most 8 column tiles, and no "
+              "per-tile statistics");
+    return SV_ERR_INVALID_ARG;
+  }
   if (part != 1) {  // whole tiles with their epilogue, and the split tiles' K ranges' raw sums
     sv_status st = launch_main(g, p, s, true);
     if (st != SV_OK || part == 0) return st;
@@ -1332,8 +1382,16 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s, i
   q.out_e4m3 = e.out_e4m3;
   q.out = e.out;
   q.ln_part = e.ln_part;
-  const long warps = long(q.n_split) * q.rows_per;
-  cudaError_t ce = launch_pdl(gemm_splitk_reduce_kernel, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, s, q);
+  q.ln_r = e.ln_r_out;
+  q.ln_aug = e.ln_aug_out;
+  q.eps = e.ln_eps;
+  cudaError_t ce;
+  if (e.ln_r_out) {  // one block per row, a warp per column tile
+    ce = launch_pdl(gemm_splitk_reduce_kernel<true>, dim3(unsigned(g.M)), dim3(unsigned(32 * p.n_tiles)), 0, s, q);
+  } else {
+    const long warps = long(q.n_split) * q.rows_per;
+    ce = launch_pdl(gemm_splitk_reduce_kernel<false>, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, s, q);
+  }
   if (ce != cudaSuccess) return cuda_fail(ce, "gemm split-K reduction launch");
   return SV_OK;
 }

@@ -87,6 +87,13 @@ struct GemmEpi {
   // Partial sums of a GEMM that splits K (GemmOperands::k_splits > 1): at least
   // gemm_splitk_ws_bytes(g) bytes, used by gemm_launch and free again when its work ends.
   float* ws = nullptr;
+  // With every tile split (k_splits > 1, n_main 0; at most 8 column tiles) the reduction
+  // can finish the row statistics itself, in place of ln_part and ln_finalize_launch:
+  // ln_r_out[m] = 1/sqrt(var + ln_eps) and ln_aug_out[m, 0..15] = (-mean_hi, -mean_hi,
+  // -mean_lo, 0, ...) over the row's N results.
+  float* ln_r_out = nullptr;
+  __half* ln_aug_out = nullptr;
+  float ln_eps = 1e-6f;
 };
 // Statistics entries per row that GemmEpi::ln_part can hold (two per column tile:
 // 1152 columns in tiles of >= 64).
