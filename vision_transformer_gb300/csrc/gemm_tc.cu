@@ -46,20 +46,18 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kSwzBytes = 128;  // one 128-byte swizzle row of K
-// Warp 0 loads, warp 1 issues the MMAs, the warps after them run the epilogue:
-// two per TMEM lane quarter, each taking every other 32-column chunk of a tile (with
-// four warps the epilogue of a K = 1152 tile took about as long as its main loop).
-// CTA pairs on E4M3 operands get three per quarter: their main loop over a K = 1152
-// tile takes half the time of the F16 one, the epilogue's work per tile is the same,
-// and with two per quarter the MMA of the 1152 -> 4304 MLP projection waited about
-// 30% of every tile for a free accumulator.
-template <bool FP8, bool PAIR>
-constexpr int epi_warps() {
-  return FP8 && PAIR ? 12 : 8;
-}
-template <bool FP8, bool PAIR>
+// Warp 0 loads, warp 1 issues the MMAs, the EPI warps after them run the epilogue:
+// 8, two per TMEM lane quarter, each taking every other 32-column chunk of a tile (with
+// four warps the epilogue of a K = 1152 tile took about as long as its main loop), or
+// 12, three per quarter: for CTA pairs on E4M3 operands (their main loop over a
+// K = 1152 tile takes half the time of the F16 one, the epilogue's work per tile is the
+// same, and with two per quarter the MMA of the 1152 -> 4304 MLP projection waited about
+// 30% of every tile for a free accumulator), and for 192-wide F16 pairs (one tile per
+// CTA pair at one image, its epilogue not overlapped: 729 x 3456 x 1152 13.0 -> 12.15
+// us). Twelve warps keep no LayerNorm statistics (those GEMMs get eight).
+template <int EPI>
 constexpr int gemm_threads() {
-  return 64 + 32 * epi_warps<FP8, PAIR>();
+  return 64 + 32 * EPI;
 }
 // Widest output tile used with CTA pairs (its TMEM: 2 x BN columns per CTA).
 constexpr int kPairMaxBn = 256;
@@ -223,14 +221,15 @@ __device__ __forceinline__ void tile_of(const Params& p, int it, int rank, int& 
 // SPLIT: 0 whole tiles only; otherwise the items from n_main on are (tile, K range) pairs
 // whose raw sums go to the split-K workspace (tmAa describes it; no LayerNorm is folded
 // into a split GEMM): 1 every item (n_main = 0), 2 whole tiles first, then split ones.
-template <int BN, bool FP8, bool PAIR, int ATOMS, int SPLIT>
-__global__ void __launch_bounds__(gemm_threads<FP8, PAIR>(), 1)
+// EPI: epilogue warps (8 or 12, see gemm_threads).
+template <int BN, bool FP8, bool PAIR, int ATOMS, int SPLIT, int EPI>
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmWt, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmAa,
                    const __grid_constant__ CUtensorMap tmWa, const __grid_constant__ CUtensorMap tmWat,
                    const Params p) {
-  constexpr int kEpiWarps = epi_warps<FP8, PAIR>();
+  constexpr int kEpiWarps = EPI;
   constexpr int kParts = kEpiWarps / 4;  // epilogue warps per TMEM lane quarter
   // With two warps per quarter the TMEM load of a warp's next chunk is issued during
   // this chunk's math. With three (128 registers a thread) each chunk loads its own:
@@ -915,10 +914,10 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const ReducePar
   }
 }
 
-template <int BN, bool FP8, bool PAIR, int ATOMS = 1, int SPLIT = 0>
+template <int BN, bool FP8, bool PAIR, int ATOMS = 1, int SPLIT = 0, int EPI = (FP8 && PAIR) ? 12 : 8>
 sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
-  using C = Cfg<BN, PAIR, ATOMS, epi_warps<FP8, PAIR>()>;
-  auto kern = gemm_tc_kernel<BN, FP8, PAIR, ATOMS, SPLIT>;
+  using C = Cfg<BN, PAIR, ATOMS, EPI>;
+  auto kern = gemm_tc_kernel<BN, FP8, PAIR, ATOMS, SPLIT, EPI>;
   // the attribute is per device: set it once on each device the kernel runs on
   static unsigned long long attr_set = 0;
   int dev = 0;
@@ -938,7 +937,7 @@ sv_status launch_bn(const GemmOperands& g, const Params& prm, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(unsigned(PAIR ? 2 * units : units), 1, 1);
-  cfg.blockDim = dim3(gemm_threads<FP8, PAIR>(), 1, 1);
+  cfg.blockDim = dim3(gemm_threads<EPI>(), 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
   // programmatic stream serialization: the prologue (barriers, TMEM, tensor-map
@@ -1278,7 +1277,8 @@ sv_status launch_main(const GemmOperands& g, const Params& p, cudaStream_t s, bo
     case 262: return launch_bn<256, false, true, 2>(g, p, s);
     case 192: return launch_bn<192, false, false>(g, p, s);
     case 193: return launch_bn<192, true, false>(g, p, s);
-    case 194: return launch_bn<192, false, true>(g, p, s);
+    case 194:  // twelve epilogue warps unless the GEMM keeps LayerNorm statistics
+      return p.ln_part ? launch_bn<192, false, true>(g, p, s) : launch_bn<192, false, true, 1, 0, 12>(g, p, s);
     case 195: return launch_bn<192, true, true>(g, p, s);
     case 128: return launch_bn<128, false, false>(g, p, s);
     case 129: return launch_bn<128, true, false>(g, p, s);
