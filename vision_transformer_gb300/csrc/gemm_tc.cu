@@ -17,14 +17,15 @@
 //               (clusters of 2) that share one M = 256 MMA (cta_group::2):
 //               each CTA stages its 128 rows of A and half of the W tile, the
 //               leader issues the MMAs, each CTA's TMEM holds its 128 rows;
-//   warps 2..   epilogue, two (three for CTA pairs on E4M3 operands) warps per
-//               TMEM lane quarter taking every second (third) 32-column
-//               chunk: tcgen05.ld of a chunk (the warp's next chunk
-//               in flight during this chunk's math), fused math, the 32 x 32
-//               result block staged in swizzled shared memory and written by a
-//               TMA store; residual blocks arrive by TMA one chunk ahead; the
-//               GEMMs that write the residual stream also leave per-tile row
-//               statistics for the next LayerNorm.
+//   warps 2..   epilogue, two warps per TMEM lane quarter taking every other
+//               32-column chunk (the warp's next chunk's tcgen05.ld in flight
+//               during this chunk's math), or three taking every third (each
+//               chunk loaded when it starts: E4M3 pairs, 192-wide F16 pairs
+//               without statistics); fused math, the 32 x 32 result block
+//               staged in swizzled shared memory and written by a TMA store;
+//               residual blocks arrive by TMA one chunk ahead; the GEMMs that
+//               write the residual stream also leave per-tile row statistics for
+//               the next LayerNorm (eight-warp epilogues).
 // Split K (long K): at small M, where the tiles would fill few SMs, every tile, and
 // otherwise the tiles of a short last wave, become (tile, K range) items; each writes
 // its raw F32 sums to a workspace and gemm_splitk_reduce_kernel adds them up in a
