@@ -216,12 +216,13 @@ sv_status sv_pack_patches(const void* images, void* pixels, int batch, int image
  *     before it is written, by the same thread).
  *   act: sv_act (applied before the residual add).
  *   out_dtype: SV_DT_F16, or SV_DT_E4M3 (codes of 16*y).
- * At small M with K >= 2048 (e.g. the 729 x 1152 x 4304 MLP-down projection of one
- * image) the GEMM may split K into ranges: two launches, the ranges' F32 partial
- * sums in a library-owned device buffer that grows to the largest need seen (a
- * cudaMalloc on such a call; freed by sv_shutdown), added in a fixed order, so
- * repeated calls give identical bits. Calls on different streams that split K
- * share that buffer and must not overlap.
+ * With K >= 2048 the GEMM may split K into ranges: at small M every output tile
+ * (e.g. the 729 x 1152 x 4304 MLP-down projection of one image), otherwise, with F16
+ * operands, the tiles of a short last round of its tile schedule (e.g. 23,328 rows).
+ * Two launches; the ranges' F32 partial sums go to a library-owned device buffer that
+ * grows to the largest need seen (a cudaMalloc on such a call; freed by sv_shutdown)
+ * and are added in a fixed order, so repeated calls give identical bits. Calls on
+ * different streams that split K share that buffer and must not overlap.
  * Requirements: M >= 1; N >= 16 and N % 16 == 0; K >= 16 and K % 16 == 0;
  * every pointer 16-byte aligned.
  * Errors: SV_ERR_INVALID_ARG, SV_ERR_OOM, SV_ERR_CUDA.
