@@ -395,6 +395,19 @@ sv_status sv_debug_fill_workspace(int batch, int gemm_dtype, int byte_value);
  */
 sv_status sv_debug_wait_timeout(unsigned int limit_us, void* stream);
 
+/*
+ * The launch plan sv_gemm_bias_act / sv_encode give an M x N x K GEMM on a GPU with
+ * `sms` SMs, computed on the host alone (no device needed): out[0..7] = tile width,
+ * CTA pairs (0/1), 128-byte rows of K per pipeline stage, width of a narrower last
+ * column tile (0: none), narrow tiles scheduled last (0/1), K ranges (1: K not split),
+ * pipeline stages per K range, and the tiles that run whole before the split ones (0
+ * with a split: every tile split). *ws_bytes (if not NULL): the split-K partial-sum
+ * workspace. max_splits: 1 as for a caller without a workspace, 8 as sv_encode and
+ * sv_gemm_bias_act use. gemm_dtype: sv_gemm_dtype. Errors: SV_ERR_INVALID_ARG.
+ */
+sv_status sv_debug_gemm_plan(int M, int N, int K, int gemm_dtype, int sms, int max_splits, int* out,
+                             size_t* ws_bytes);
+
 /* Stages of the forward pass that sv_debug_encode_stage can stop after. */
 typedef enum {
   SV_STAGE_PATCH = 0,     /* X after the patch embedding: f16 [batch*tokens, width] */

@@ -55,6 +55,7 @@ SIGNATURES = [
     ("sv_profile_read", _I, [_I, _DP, _DP, _DP, _LLP]),
     ("sv_debug_fill_workspace", _I, [_I, _I, _I]),
     ("sv_debug_wait_timeout", _I, [ctypes.c_uint, _VP]),
+    ("sv_debug_gemm_plan", _I, [_I, _I, _I, _I, _I, _I, _IP, ctypes.POINTER(ctypes.c_size_t)]),
     ("sv_debug_encode_stage", _I, [_VP, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
     ("sv_shutdown", None, []),
 ]
@@ -247,6 +248,15 @@ def sv_profile_read(kind: int) -> dict:
 
 def sv_debug_fill_workspace(batch: int, gemm_dtype: int, byte_value: int):
     _check("sv_debug_fill_workspace", load().sv_debug_fill_workspace(batch, gemm_dtype, byte_value))
+
+
+def sv_debug_gemm_plan(M: int, N: int, K: int, gemm_dtype: int = 0, sms: int = 152, max_splits: int = 8) -> dict:
+    out = (ctypes.c_int * 8)()
+    ws = ctypes.c_size_t(0)
+    _check("sv_debug_gemm_plan", load().sv_debug_gemm_plan(M, N, K, gemm_dtype, sms, max_splits, out,
+                                                           ctypes.byref(ws)))
+    keys = ("bn", "pairs", "atoms", "tail_n", "tail_last", "k_splits", "kb_split", "n_main")
+    return dict(zip(keys, list(out)), ws_bytes=ws.value)
 
 
 def sv_debug_wait_timeout(limit_us: int, stream=None):

@@ -1024,10 +1024,10 @@ sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int
 // ones measured on GB300 for 23,328-row GEMMs with the copies and epilogue
 // running (TFLOP/s at 256 / 192 / 128 / 64 columns: about 1780 / 1480 / 1000 /
 // 600): wide tiles win whenever there are enough of them to fill the SMs.
-int gemm_pick_bn(int M, int N, int K, bool pair, double* t_best) {
+int gemm_pick_bn(int M, int N, int K, bool pair, double* t_best, int sms) {
   const int cand[4] = {256, 192, 128, 64};
   const double rate[4] = {1780.0, 1480.0, 1000.0, 600.0};
-  const int sms = num_sms() > 0 ? num_sms() : 148;
+  if (sms <= 0) sms = 148;
   int best = 256;
   double best_t = 1e30;
   const int mt = (M + kBM - 1) / kBM;
@@ -1056,9 +1056,8 @@ namespace {
 // while E4M3 729 rows (14.1 vs 14.4 split) and 1458 rows (15.8 vs 19.6) stay whole.
 // Returns the number of K ranges (1: no split); sets *bn and *mc for the split layout.
 int pick_splits(int M, int N, int K, int fp8, bool allow_pair, int max_splits, double t_unsplit, int* bn,
-                int* mc) {
+                int* mc, int sms) {
   constexpr double kReduceCost = 125.0;
-  const int sms = num_sms() > 0 ? num_sms() : 148;
   if (max_splits < 2 || K < 2048) return 1;
   const int mt = (M + kBM - 1) / kBM;
   const bool pair = allow_pair && mt >= 2 && sms >= 2;
@@ -1088,9 +1087,8 @@ int pick_splits(int M, int N, int K, int fp8, bool allow_pair, int max_splits, d
 // tile (128 columns, 93,312 rows) no gain, and E4M3 99.2 -> 102.2 us (its main loop is
 // short against the epilogue); so F16 only, and only when the round shortens by more than
 // three reductions (gemm_pick_bn's time units, as pick_splits).
-void pick_tail_split(GemmOperands* g, int k_blocks) {
+void pick_tail_split(GemmOperands* g, int k_blocks, int sms) {
   constexpr double kReduceCost = 125.0;
-  const int sms = num_sms() > 0 ? num_sms() : 148;
   if (g->fp8 || g->K < 2048 || g->bn != 256 || g->atoms != 1) return;
   const int mt = (g->M + kBM - 1) / kBM, units = g->mc ? (mt + 1) / 2 : mt;
   const int n_tiles = (g->N + g->bn - 1) / g->bn, n_full = g->tail_n ? n_tiles - 1 : n_tiles;
@@ -1114,8 +1112,9 @@ void pick_tail_split(GemmOperands* g, int k_blocks) {
   g->n_main = items - rem;
 }
 
-// Tile, pairing, stage and split choices for an M x N x K GEMM (no tensor maps).
-void gemm_choose(GemmOperands* g, int M, int N, int K, int fp8, bool allow_pair, int max_splits) {
+// Tile, pairing, stage and split choices for an M x N x K GEMM on `sms` SMs (no tensor maps).
+void gemm_choose(GemmOperands* g, int M, int N, int K, int fp8, bool allow_pair, int max_splits, int sms) {
+  if (sms <= 0) sms = 148;
   g->M = M;
   g->N = N;
   g->K = K;
@@ -1128,11 +1127,11 @@ void gemm_choose(GemmOperands* g, int M, int N, int K, int fp8, bool allow_pair,
   // halves the W part. Measured on the 27-layer encoder: about 2% faster on the MLP and
   // QKV GEMMs, and with two swizzle rows of K per stage 1% per step faster on the
   // 1152 x 1152 output projection (batch 32 and 128).
-  g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && num_sms() >= 2 && (K >= 1024 || N >= 2048);
+  g->mc = allow_pair && (M + kBM - 1) / kBM >= 2 && sms >= 2 && (K >= 1024 || N >= 2048);
   double t_unsplit = 0.0;
-  g->bn = gemm_pick_bn(M, N, K, g->mc, &t_unsplit);
+  g->bn = gemm_pick_bn(M, N, K, g->mc, &t_unsplit, sms);
   if (g->mc && g->bn > kPairMaxBn) g->bn = kPairMaxBn;
-  g->k_splits = pick_splits(M, N, K, fp8, allow_pair, max_splits, t_unsplit, &g->bn, &g->mc);
+  g->k_splits = pick_splits(M, N, K, fp8, allow_pair, max_splits, t_unsplit, &g->bn, &g->mc, sms);
   // two swizzle rows of K per stage for 256-wide F16 CTA-pair tiles over a short K that
   // they divide (see Cfg). Not for E4M3: over K = 1152 half of the last stage would be
   // empty, and with the E4M3 pairs' wider epilogue only two 64 KB stages would fit.
@@ -1154,7 +1153,7 @@ void gemm_choose(GemmOperands* g, int M, int N, int K, int fp8, bool allow_pair,
     // encoder's GEMMs: a 3% shorter schedule did not pay for the second pass over A.)
     const int mu = g->mc ? ((M + kBM - 1) / kBM + 1) / 2 : (M + kBM - 1) / kBM;
     const int nt_all = (N + g->bn - 1) / g->bn, nf = nt_all - 1;
-    const int units = g->mc ? num_sms() / 2 : num_sms();
+    const int units = g->mc ? sms / 2 : sms;
     const long items = long(mu) * nt_all;
     auto makespan = [&](bool tail_last) {
       long worst = 0;
@@ -1173,7 +1172,7 @@ void gemm_choose(GemmOperands* g, int M, int N, int K, int fp8, bool allow_pair,
   }
   const int bk = (fp8 ? kSwzBytes : kSwzBytes / 2) * g->atoms;
   const int k_blocks = (K + bk - 1) / bk;
-  if (g->k_splits == 1 && max_splits > 1) pick_tail_split(g, k_blocks);
+  if (g->k_splits == 1 && max_splits > 1) pick_tail_split(g, k_blocks, sms);
   if (g->k_splits > 1) {  // equal ranges of whole stages; no range is empty
     g->kb_split = (k_blocks + g->k_splits - 1) / g->k_splits;
     g->k_splits = (k_blocks + g->kb_split - 1) / g->kb_split;
@@ -1191,13 +1190,13 @@ size_t gemm_splitk_ws_bytes(const GemmOperands& g) {
 
 size_t gemm_splitk_ws_bytes_for(int M, int N, int K, int fp8, int max_splits) {
   GemmOperands g;
-  gemm_choose(&g, M, N, K, fp8, true, max_splits);
+  gemm_choose(&g, M, N, K, fp8, true, max_splits, num_sms());
   return gemm_splitk_ws_bytes(g);
 }
 
 sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8,
                        bool allow_pair, int max_splits) {
-  gemm_choose(g, M, N, K, fp8, allow_pair, max_splits);
+  gemm_choose(g, M, N, K, fp8, allow_pair, max_splits, num_sms());
   sv_status st = gemm_operand_map(&g->ta, A, M, K, fp8, kBM);
   if (st != SV_OK) return st;
   st = gemm_operand_map(&g->tw, W, N, K, fp8, g->mc ? g->bn / 2 : g->bn);
@@ -1398,3 +1397,20 @@ sv_status gemm_launch(const GemmOperands& g, const GemmEpi& e, cudaStream_t s, i
 }
 
 }  // namespace sv
+
+// The tile, pairing, stage and split choices for an M x N x K GEMM on `sms` SMs, as
+// gemm_prepare makes them with max_splits (a host-only computation, for tests).
+extern "C" sv_status sv_debug_gemm_plan(int M, int N, int K, int gemm_dtype, int sms, int max_splits, int* out,
+                                        size_t* ws_bytes) {
+  if (M < 1 || N < 16 || K < 16 || N % 16 || K % 16 || (gemm_dtype != 0 && gemm_dtype != 1) || sms < 1 ||
+      max_splits < 1 || !out) {
+    sv::set_error("sv_debug_gemm_plan: bad arguments");
+    return SV_ERR_INVALID_ARG;
+  }
+  sv::GemmOperands g;
+  sv::gemm_choose(&g, M, N, K, gemm_dtype, true, max_splits, sms);
+  const int v[8] = {g.bn, g.mc, g.atoms, g.tail_n, g.tail_last, g.k_splits, g.kb_split, g.n_main};
+  for (int i = 0; i < 8; ++i) out[i] = v[i];
+  if (ws_bytes) *ws_bytes = sv::gemm_splitk_ws_bytes(g);
+  return SV_OK;
+}

@@ -127,7 +127,7 @@ struct GemmOperands {
 // Tensor map of a K-major operand [rows, K] (row stride = K elements) with the
 // 128-byte swizzle the GEMM expects, box [box_rows, 128 bytes].
 sv_status gemm_operand_map(CUtensorMap* m, const void* ptr, int rows, int K, int fp8, int box_rows);
-int gemm_pick_bn(int M, int N, int K, bool mc, double* t_best = nullptr);
+int gemm_pick_bn(int M, int N, int K, bool mc, double* t_best, int sms);
 // allow_pair = false keeps single-CTA tiles; max_splits > 1 lets a small-M, long-K GEMM
 // split K into up to that many ranges (the caller then provides GemmEpi::ws).
 sv_status gemm_prepare(GemmOperands* g, const void* A, const void* W, int M, int N, int K, int fp8,
