@@ -50,9 +50,9 @@ def flops_per_image(layers: int = L27) -> float:
 # dram__bytes_write.sum from one ncu capture of the four encoder GEMMs of a layer at
 # batch 32, F16 (QKV, output projection, MLP up, MLP down; their mean), valid only for
 # the kernel sources it was taken on (first 16 hex digits of sha256 of each file).
-GEMM_TRAFFIC = {"batch": 32, "bytes_per_launch": 213.3e6,
+GEMM_TRAFFIC = {"batch": 32, "bytes_per_launch": 213.7e6,
                 "weight_bytes_per_launch": 7.6e6,  # mean F16 weight bytes of the four
-                "sources": {"vision_transformer_gb300/csrc/gemm_tc.cu": "c4ee66bcf9ff022c",
+                "sources": {"vision_transformer_gb300/csrc/gemm_tc.cu": "54a41cc577e35712",
                             "vision_transformer_gb300/csrc/ptx.cuh": "0d440f4ccbdf05b8"}}
 
 
