@@ -408,6 +408,27 @@ sv_status sv_debug_wait_timeout(unsigned int limit_us, void* stream);
 sv_status sv_debug_gemm_plan(int M, int N, int K, int gemm_dtype, int sms, int max_splits, int* out,
                              size_t* ws_bytes);
 
+/*
+ * Attention kernels ("SigLIP ViT benchmark", attention paragraph: softmax(Q K^T / sqrt(72)) V
+ * per head). Every attention launch (sv_attention*, sv_encode) runs one of two kernels with
+ * the same arithmetic: 1 = items of two 128-query tiles per CTA, 2 = items of one 128-query
+ * tile with three score tiles in tensor memory. By size (choice 0, the default) the second
+ * runs when all of a launch's one-tile items, ceil(tokens / 128) x heads x batch, fit in one
+ * round of the SMs (one image of 729 tokens and 16 heads: 96 items), the first otherwise.
+ * sv_debug_attention_kernel(1 or 2) forces one kernel for later launches of this process,
+ * for tests that cover both on the same sizes; step graphs that sv_encode captured before
+ * keep the kernel they were captured with. Errors: SV_ERR_INVALID_ARG (choice not 0, 1, 2).
+ */
+sv_status sv_debug_attention_kernel(int choice);
+
+/*
+ * The kernel (*kernel: 1 or 2, as above) and the number of persistent CTAs (*grid) that an
+ * attention launch over `batch` images of `tokens` tokens and `heads` heads takes on a GPU
+ * with `sms` SMs under the current choice; computed on the host alone (no device needed).
+ * Errors: SV_ERR_INVALID_ARG (a size < 1, or a NULL output).
+ */
+sv_status sv_debug_attention_plan(int batch, int tokens, int heads, int sms, int* kernel, int* grid);
+
 /* Stages of the forward pass that sv_debug_encode_stage can stop after. */
 typedef enum {
   SV_STAGE_PATCH = 0,     /* X after the patch embedding: f16 [batch*tokens, width] */

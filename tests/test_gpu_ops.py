@@ -218,6 +218,15 @@ def test_pack_patches_bit_exact(sv, B, side, C, patch):
     assert np.array_equal(host(out).astype(np.float16).view(np.uint16), ref.view(np.uint16))
 
 
+@pytest.fixture(params=[1, 2], ids=["two_tile_items", "score_slots"])
+def attn_kernel(request, sv):
+    """Runs the test on each attention kernel (1: items of two 128-query tiles, 2: one
+    tile with three score slots in tensor memory); launches choose by size otherwise."""
+    sv.sv_debug_attention_kernel(request.param)
+    yield request.param
+    sv.sv_debug_attention_kernel(0)
+
+
 def _attn_ref(qkv, H):
     D = H * 72
     return oracle.attention(qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:], H, 72)
@@ -225,7 +234,7 @@ def _attn_ref(qkv, H):
 
 @pytest.mark.parametrize("B,H,T,sharp", [(1, 2, 4, 1.0), (2, 16, 729, 1.0), (1, 3, 200, 3.0), (8, 16, 729, 2.0),
                                          (1, 1, 129, 1.0), (1, 2, 1, 1.0), (3, 4, 300, 1.5)])
-def test_attention(sv, B, H, T, sharp):
+def test_attention(sv, attn_kernel, B, H, T, sharp):
     D = H * 72
     qkv = synth.normal(80 + T, 1, (B, T, 3 * D))
     qkv[..., :D] = (qkv[..., :D].astype(np.float32) * sharp).astype(np.float16)
@@ -238,11 +247,11 @@ def test_attention(sv, B, H, T, sharp):
 
 
 @pytest.mark.parametrize("qk8", [0, 1])
-def test_attention_repeats_bit_identical(sv, qk8):
-    """The attention kernel's products reuse tensor-memory columns in issue order (the
+def test_attention_repeats_bit_identical(sv, attn_kernel, qk8):
+    """The attention kernels' products reuse tensor-memory columns in issue order (the
     next S product overwrites the P values the P V product reads); a race there would
     show up as outputs that differ between identical launches. 12 launches at the batch-32
-    size (1536 work items over the persistent CTAs) must give the same bits."""
+    size (1536 or 3072 work items over the persistent CTAs) must give the same bits."""
     B, H, T = 32, 16, 729
     D = H * 72
     qkv = dev_f16(synth.normal(95, 1, (B, T, 3 * D)))
@@ -256,7 +265,7 @@ def test_attention_repeats_bit_identical(sv, qk8):
 
 
 @pytest.mark.parametrize("B,H,T,stride", [(2, 16, 729, 80), (1, 3, 200, 72), (3, 4, 300, 96), (1, 2, 1, 80)])
-def test_attention_heads(sv, B, H, T, stride):
+def test_attention_heads(sv, attn_kernel, B, H, T, stride):
     """Per-head Q, K, V [B, H, T, stride]: the columns past the head width are NaN and
     never read; the result equals the attention of the same values in the fused
     layout, and the default scale (0 -> 1/sqrt(72)) equals the explicit one."""
@@ -282,7 +291,7 @@ def test_attention_heads(sv, B, H, T, stride):
 
 @pytest.mark.parametrize("B,H,T,sharp", [(1, 2, 4, 1.0), (2, 16, 729, 1.0), (1, 3, 200, 3.0), (3, 4, 300, 1.5),
                                          (1, 1, 129, 1.0), (1, 2, 1, 1.0)])
-def test_attention_qk_e4m3(sv, B, H, T, sharp):
+def test_attention_qk_e4m3(sv, attn_kernel, B, H, T, sharp):
     """FP8 score products ("FP8 attention and resident image/embedding transfers",
     Projected attention): both sides round the same F16 Q and K values to E4M3 at
     scale 2^-4, so the F16 attention tolerance holds against the oracle's QK-rounding
@@ -301,7 +310,7 @@ def test_attention_qk_e4m3(sv, B, H, T, sharp):
         assert np.abs(got - _attn_ref(qkv, H)).max() > 4 * RT * vmax
 
 
-def test_attention_e4m3_output_and_poisoned_neighbours(sv):
+def test_attention_e4m3_output_and_poisoned_neighbours(sv, attn_kernel):
     """Rows past an image's last token and columns outside a head are never
     read as data: the qkv buffer sits inside NaN-filled memory and the output
     buffer starts as NaN."""

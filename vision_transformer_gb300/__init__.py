@@ -56,6 +56,8 @@ SIGNATURES = [
     ("sv_debug_fill_workspace", _I, [_I, _I, _I]),
     ("sv_debug_wait_timeout", _I, [ctypes.c_uint, _VP]),
     ("sv_debug_gemm_plan", _I, [_I, _I, _I, _I, _I, _I, _IP, ctypes.POINTER(ctypes.c_size_t)]),
+    ("sv_debug_attention_kernel", _I, [_I]),
+    ("sv_debug_attention_plan", _I, [_I, _I, _I, _I, _IP, _IP]),
     ("sv_debug_encode_stage", _I, [_VP, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
     ("sv_shutdown", None, []),
 ]
@@ -257,6 +259,17 @@ def sv_debug_gemm_plan(M: int, N: int, K: int, gemm_dtype: int = 0, sms: int = 1
                                                            ctypes.byref(ws)))
     keys = ("bn", "pairs", "atoms", "tail_n", "tail_last", "k_splits", "kb_split", "n_main")
     return dict(zip(keys, list(out)), ws_bytes=ws.value)
+
+
+def sv_debug_attention_kernel(choice: int) -> None:
+    _check("sv_debug_attention_kernel", load().sv_debug_attention_kernel(choice))
+
+
+def sv_debug_attention_plan(batch: int, tokens: int, heads: int, sms: int = 152) -> dict:
+    kernel, grid = ctypes.c_int(0), ctypes.c_int(0)
+    _check("sv_debug_attention_plan", load().sv_debug_attention_plan(batch, tokens, heads, sms, ctypes.byref(kernel),
+                                                                     ctypes.byref(grid)))
+    return {"kernel": kernel.value, "grid": grid.value}
 
 
 def sv_debug_wait_timeout(limit_us: int, stream=None):
