@@ -124,11 +124,20 @@ def _stage(sv, pix_dev, layers, stage, cols):
 def test_encoder_batch1_split_mlp_down_and_statistics(sv, two_layers):
     """One image, F16: the MLP-down projection splits K. Its reduction's output
     (X after layer 1) and its row statistics (consumed by layer 2's LayerNorm,
-    folded into the QKV projection) against the oracle on the GPU's own inputs."""
+    folded into the QKV projection) against the oracle on the GPU's own inputs;
+    and layer 1's LN1 + QKV and LN2 + MLP up, whose statistics come from the patch
+    embedding's and the output projection's epilogues at this size."""
     p, pix_dev = two_layers
     f16 = lambda a: np.asarray(a, dtype=np.float64).astype(np.float16)
+    x0 = _stage(sv, pix_dev, 1, sv.SV_STAGE_PATCH, D)
+    qkv1 = _stage(sv, pix_dev, 1, sv.SV_STAGE_QKV, 3 * D)
+    ref = oracle.linear(oracle.layernorm(f16(x0), p["ln1_g"][0], p["ln1_b"][0]), p["qkv_w"][0], p["qkv_b"][0])
+    assert_close(qkv1, ref, RT, 2 * RT * _scale(ref), "layer 1 LN1 (statistics from the patch GEMM) + QKV")
     hh = _stage(sv, pix_dev, 1, sv.SV_STAGE_MLP_UP, F)
     x1_in = _stage(sv, pix_dev, 1, sv.SV_STAGE_OUT_PROJ, D)
+    ref = oracle.linear(oracle.layernorm(f16(x1_in), p["ln2_g"][0], p["ln2_b"][0]), p["fc1_w"][0], p["fc1_b"][0],
+                        act=1)
+    assert_close(hh, ref, RT, 2 * RT * _scale(ref), "layer 1 LN2 (statistics from the output projection) + MLP up")
     x1 = _stage(sv, pix_dev, 1, sv.SV_STAGE_MLP_DOWN, D)
     ref = oracle.linear(f16(hh), p["fc2_w"][0], p["fc2_b"][0], residual=f16(x1_in))
     assert_close(x1, ref, RT, RT * _scale(ref), "layer 1 MLP down (split K) + residual")
