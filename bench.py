@@ -221,6 +221,7 @@ def run_reference(args, world, rank):
 # The other configurations of the throughput sweep and the latency cases, timed in the
 # same run after the main workload (single-GPU runs): (name, batch, gemm dtype).
 EXTRA_CONFIGS = (("b1_f16", 1, "f16"), ("b2_e4m3", 2, "e4m3"), ("b32_f16", 32, "f16"), ("b128_e4m3", 128, "e4m3"))
+CONFIG_MIN_S = 0.25  # seconds of warm-up and of timed steps at least, per configuration
 
 
 def time_config(vt, torch, dev, stream, batch, dtype, steps, warmup, local):
@@ -230,10 +231,19 @@ def time_config(vt, torch, dev, stream, batch, dtype, steps, warmup, local):
     pix = torch.empty(batch, T, P, dtype=torch.float16, device=dev)
     vt.sv_make_pixels(3000, batch, pix)
     out = torch.empty(batch, 1, D, dtype=torch.float16, device=dev)
-    for _ in range(warmup):
+    # Warm-up of at least `warmup` steps and about 0.25 s, each step waited for, so that the
+    # clocks leave the power state of the workload timed before (a one-image step takes
+    # about 2 ms); then at least `steps` timed steps covering about 0.25 s as well.
+    t0, n_warm, step_s = time.perf_counter(), 0, 0.0
+    while n_warm < warmup or time.perf_counter() - t0 < CONFIG_MIN_S:
+        t1 = time.perf_counter()
         vt.sv_encode(pix, out, batch, L27, gdt, stream)
-    vt.sv_sync(stream)
+        vt.sv_sync(stream)
+        step_s = time.perf_counter() - t1
+        n_warm += 1
     torch.cuda.synchronize(dev)
+    steps = max(steps, int(CONFIG_MIN_S / max(step_s, 1e-4)) + 1)
+    warmup = n_warm
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     with ClockSampler(local) as clk:
         ev[0].record(stream)
