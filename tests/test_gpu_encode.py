@@ -149,6 +149,23 @@ def test_27_layers_e4m3_batch2(sv, ref27):
     assert cosine_rows(got, ref_q).min() >= 0.995
 
 
+@pytest.mark.parametrize("flags", [0, 2])
+def test_27_layers_e4m3_batch1(sv, so400m, ref27, flags):
+    """One image with E4M3 GEMMs, with F16 or E4M3 attention scores (flags 2): at this
+    size attention runs as one-tile items (the small-grid kernel) and writes E4M3 rows
+    for the output projection. The bounds of the two-image tests."""
+    pix, ref, ref_q = ref27
+    D = sv.sv_model_dims()["width"]
+    out = torch.empty(1, 1, D, dtype=torch.float16, device="cuda")
+    sv.sv_encode_ex(torch.from_numpy(pix[:1]).cuda(), out, 1, 27, 1, flags)
+    sv.sv_sync()
+    got = host(out).reshape(1, -1)
+    assert cosine_rows(got, ref[:1]).min() >= 0.99
+    assert np.abs(got - ref[:1]).max() <= 0.5
+    ref_mode = ref_q[:1] if not flags else so400m.encode(pix[:1], fp8=True, fp8_attention=True)
+    assert cosine_rows(got, ref_mode).min() >= 0.995
+
+
 def test_27_layers_e4m3_fp8_attention_batch2(sv, so400m, ref27):
     """E4M3 GEMMs and FP8 attention products ("FP8 attention and resident
     image/embedding transfers", Full 27-layer ViT: against the unquantised
