@@ -277,7 +277,8 @@ sv_status sv_ln_gemm(const void* x, const void* gamma, const void* beta, float e
  * o_h = softmax(scale * Q_h K_h^T) V_h; scale <= 0 selects 1 / sqrt(head_dim)
  * (scaled dot-product attention). Requirements: head_dim == 72, tokens >= 1,
  * heads >= 1. The call keeps a scratch buffer (the head-blocked copy of qkv) that
- * grows to the largest call and is freed by sv_shutdown.
+ * grows to the largest call and is freed by sv_shutdown. One of two kernels with the
+ * same arithmetic runs, chosen by the launch's size (sv_debug_attention_plan).
  */
 sv_status sv_attention(const void* qkv, void* o, int batch, int heads, int tokens, int head_dim, float scale,
                        int out_dtype, void* stream);
